@@ -1,0 +1,438 @@
+"""Decode-attention benchmark: KV GB/s and tokens/s of one decode step.
+
+Workload: 4 requests x 31,744-token histories, 16 layers, 24 query / 4 KV heads,
+head_dim 256, bf16 K/V in 64-token pages (4,096 B per token per layer), one
+32K tile per request, FP32 LSE merge.  A step is, for all 16 layers: write the
+new token's row into its page, paged GQA decode attention with per-tile LSE,
+LSE merge.
+
+  value  resident route: history already in HBM; KV GB/s = sum_r L_r x 4,096 B
+         x 16 layers per step / step time.
+  e2e    host-staged route through the same C-ABI with host buffers: per step
+         Q and the new rows go host->device, every layer's history is staged
+         from pinned host memory into a 2-slot device arena, the tail rows are
+         written back, and the outputs come back to the host.
+  roofline  the attention kernel alone: algorithmic bytes per launch / mean
+         launch time (CUDA events on the launching stream), against the
+         measured HBM copy bandwidth.
+  cpu_baseline  the fp64 NumPy oracle on a bounded sample on the host cores.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn KV GB/s (% of HBM peak) and tokens/s at 32K-262K ctx, 1 GB300"
+UNIT = "GB/s"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_kernel_4x31744.md")
+KERNEL_SOURCE = os.path.join(ROOT, "paged_decode_attention_attn_gb300", "csrc", "decode_attn.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cuda-core", action="store_true",
+                    help="time the CUDA-core attention kernel instead of the tensor-core one")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-workers", type=int, default=0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_init(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+
+    def start(self):
+        self._thread = threading.Thread(target=self._run, daemon=True)
+        self._thread.start()
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                out = subprocess.run(
+                    ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits"], capture_output=True, text=True,
+                    timeout=5).stdout.strip()
+                if out:
+                    self.samples.append([x.strip() for x in out.split(",")])
+            except Exception:
+                pass
+            self._stop.wait(0.2)
+
+    def stop(self):
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=10)
+        sm = []
+        mx = 0.0
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in self.samples:
+            try:
+                sm.append(float(s[0]))
+                mx = max(mx, float(s[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, s[4:8]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def recorded_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel source as it is now (else None)."""
+    try:
+        src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+        fields = {}
+        for line in open(TRAFFIC_FILE):
+            if ":" in line and line.strip().startswith("- "):
+                k, v = line.strip()[2:].split(":", 1)
+                fields[k.strip()] = v.strip().strip("`")
+        if fields.get("kernel_source_sha256") != src:
+            return None
+        return int(fields["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (the cpu_baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def _oracle_task(args):
+    """One (layer, request) of the workload through the fp64 oracle; returns
+    (seconds, kv_bytes).  Inputs are seeded bf16 N(0,1) with the workload's
+    shapes; the same page layout and page-table indirection as the GPU path."""
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    import numpy as np
+    import oracle
+    seed, length, n_kv, d, pt = args
+    rng = np.random.default_rng(seed)
+    n_pages = -(-length // pt)
+    row = 2 * n_kv * d
+    f32 = rng.standard_normal((n_pages, pt, row), dtype=np.float32)
+    u = f32.view(np.uint32)
+    pool = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)   # round to nearest even
+    q = ((rng.standard_normal((6 * n_kv, d), dtype=np.float32).view(np.uint32) + 0x7FFF)
+         >> 16).astype(np.uint16)
+    table = rng.permutation(n_pages).astype(np.int32)
+    del f32, u
+    t0 = time.perf_counter()
+    oracle.decode_layer(q, pool, table, length, [(0, length)], 1.0 / 16, n_kv, d, pt)
+    return time.perf_counter() - t0, length * row * 2
+
+
+def oracle_sample(n_tasks, workers, length=31744):
+    import multiprocessing as mp
+    os.environ["OPENBLAS_NUM_THREADS"] = "1"
+    os.environ["OMP_NUM_THREADS"] = "1"
+    os.environ["MKL_NUM_THREADS"] = "1"
+    tasks = [(1000 + i, length, 4, 256, 64) for i in range(n_tasks)]
+    ctx = mp.get_context("spawn")
+    t0 = time.perf_counter()
+    with ctx.Pool(workers) as pool:
+        res = pool.map(_oracle_task, tasks)
+    wall = time.perf_counter() - t0
+    busy = sum(r[0] for r in res)
+    kv = sum(r[1] for r in res)
+    return dict(kv_bytes=kv, wall_s=wall, busy_s=busy, tasks=n_tasks, workers=workers)
+
+
+def cpu_baseline_dict(workers_arg):
+    workers = workers_arg or min(8, cpu_cores())
+    s = oracle_sample(n_tasks=2 * workers, workers=workers)
+    gbs = s["kv_bytes"] / s["busy_s"] * workers / 1e9
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": workers, "kind": "oracle",
+            "sample": (f"{s['tasks']} (layer, request) pairs of 31,744 tokens (4 KV heads x 256, "
+                       f"bf16 pages) through the fp64 NumPy oracle, {workers} single-threaded "
+                       f"spawn workers; {s['busy_s']:.1f} s of CPU time, {s['wall_s']:.1f} s wall")}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    workers = args.cpu_workers or min(8, cpu_cores())
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_sample(n_tasks=workers, workers=workers)
+    times, kv = [], 0
+    for _ in range(args.steps):
+        s = oracle_sample(n_tasks=workers, workers=workers)
+        times.append(s["wall_s"])
+        kv = s["kv_bytes"]
+    total_t = sum(times)
+    value = kv * args.steps / total_t / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * total_t / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": "4x31744-16layers (sampled: one (layer, request) per worker "
+                                   "per step)", "ctx": 31744, "batch": 4, "layers": 16},
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": workers,
+                             "kind": "oracle",
+                             "sample": f"{workers} (layer, request) pairs of 31,744 tokens per "
+                                       f"step, {workers} single-threaded spawn workers"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import numpy as np
+    import torch
+    rank, world, local = dist_init(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from paged_decode_attention_attn_gb300 import binding as B
+    from paged_decode_attention_attn_gb300 import decode as D
+    from paged_decode_attention_attn_gb300 import workloads as wl
+
+    w = wl.four_requests_31744()
+    t = wl.materialize(w, dev)
+    geo = w.geometry
+    kv_bytes = w.kv_bytes_per_step()
+    kv_bytes_layer = kv_bytes // w.n_layers
+    stream = torch.cuda.current_stream(dev)
+    res = D.ResidentDecode(w, t, cuda_core=args.cuda_core, stream=stream)
+
+    # ---- resident route: value + roofline ----
+    n_ev = args.steps * w.n_layers
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(n_ev)]
+
+    def resident_step(step_idx):
+        o = res.o
+        for i in range(w.n_layers):
+            B.kv_append_rows(t["pool"][i], t["page_table"], t["positions"], t["new_rows"][i],
+                             status=res.status, stream=stream)
+            if step_idx is not None:
+                ev[step_idx * w.n_layers + i][0].record(stream)
+            B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], res.tiles,
+                                    geo.scale, o.tile_out[i], o.tile_lse[i], res.workspace,
+                                    stream=stream, cuda_core=args.cuda_core)
+            if step_idx is not None:
+                ev[step_idx * w.n_layers + i][1].record(stream)
+            B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
+                        o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
+                        o.lse[i], stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        resident_step(None)
+    torch.cuda.synchronize(dev)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for k in range(args.steps):
+        resident_step(k)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    elapsed_ms = start.elapsed_time(end)
+    # attention-kernel launch times, recorded around each launch in the timed region
+    kernel_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    status = res.kernel_status()
+    if status != 0:
+        raise RuntimeError(f"kernel status word {status:#x}")
+    max_ms = max_over_ranks(elapsed_ms, world)
+    step_ms = max_ms / args.steps
+    value = world * kv_bytes * args.steps / (max_ms / 1e3) / 1e9
+    tokens_per_s = world * w.batch * args.steps / (max_ms / 1e3)
+    peak, peak_kind = hbm_peak()
+    kern_ms = statistics.mean(kernel_ms)
+    achieved = kv_bytes_layer / (kern_ms / 1e3) / 1e9
+
+    # ---- staged route, end to end through host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, w, t, dev, D, B)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_dict(args.cpu_workers)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "batch": w.batch, "ctx": int(w.lengths[0]),
+                       "layers": w.n_layers, "heads": "24q/4kv", "head_dim": 256,
+                       "page_tokens": 64, "tiles_per_request": w.n_tiles,
+                       "route": "resident", "parallelism": f"replicas x{world}",
+                       "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step)",
+                       "kernel": "cuda-core fp32" if args.cuda_core
+                       else "tensor-core mma.sync bf16 + TMA pipeline",
+                       "accumulate": "fp32"},
+            "tokens_per_s": round(tokens_per_s, 1),
+            "pct_of_hbm_peak": round(100 * value / peak, 2),
+            "gpu_launches": 3 * w.n_layers * args.steps,
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": round(achieved / peak, 4), "traffic": recorded_traffic(),
+                         "kernel": "paged_decode_kernel",
+                         "bytes_per_launch": kv_bytes_layer,
+                         "mean_launch_ms": round(kern_ms, 5)},
+            "clocks": clk,
+        }
+        if e2e is not None:
+            line["e2e"] = e2e
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_e2e(args, w, t, dev, D, B):
+    """Staged route: host-owned history, host Q / new rows in, outputs out."""
+    import torch
+    geo = w.geometry
+    host = D.HostHistory(w, t)
+    compute = torch.cuda.current_stream(dev)
+    st = D.StagedDecode(w, t, host, n_slots=2, compute_stream=compute)
+    q_host = t["q"].cpu().pin_memory()
+    rows_host = t["new_rows"].cpu().pin_memory()
+    out_host = torch.empty(st.o.out.shape, dtype=torch.float32).pin_memory()
+    lse_host = torch.empty(st.o.lse.shape, dtype=torch.float32).pin_memory()
+    q_dev, rows_dev = t["q"], t["new_rows"]
+
+    def step():
+        q_dev.copy_(q_host, non_blocking=True)
+        rows_dev.copy_(rows_host, non_blocking=True)
+        st.step()
+        out_host.copy_(st.o.out, non_blocking=True)
+        lse_host.copy_(st.o.lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    st.drain()
+    torch.cuda.synchronize(dev)
+    steps = max(3, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    st.drain()
+    torch.cuda.synchronize(dev)
+    secs = time.perf_counter() - t0
+    if st.kernel_status() != 0:
+        raise RuntimeError("staged route kernel status non-zero")
+    stats = st.handle.stats()
+    staged_per_step = stats.staged_bytes // stats.stage_generation * w.n_layers
+    h2d = q_host.numel() * 2 + rows_host.numel() * 2 + staged_per_step
+    d2h = out_host.numel() * 4 + lse_host.numel() * 4 + w.n_layers * w.batch * geo.row_bytes
+    kv = w.kv_bytes_per_step()
+    res = {"value": round(kv * steps / secs / 1e9, 2), "unit": UNIT,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "route": "host-staged, 2 arena slots, tail write-back",
+           "ms_per_step": round(1e3 * secs / steps, 3),
+           "h2d_GBps": round(staged_per_step * steps / secs / 1e9, 2), "steps": steps}
+    st.close()
+    host.close()
+    return res
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,290 @@
+/*
+ * pagedattn.h -- C ABI of libpagedattn: paged GQA decode attention with a
+ * per-tile log-sum-exp, an FP32 LSE merge, and a staging arena that moves a
+ * layer's KV history from pinned host memory into bounded device slots.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [KVE-exact]  "KV-cache engineering", section "Exact recent pages, compact
+ *                older pages": tiles each return a normalised output and its
+ *                log-sum-exp; an FP32 merge weights each by exp(LSE_i - max),
+ *                sums, divides by the summed weights, LSE = max + log(sum).
+ *   [KVE-bus]    "KV-cache engineering", section "Costing the bus before
+ *                changing anything": pinned host memory owns the cache, the
+ *                device keeps a bounded working set, the exact path re-reads
+ *                every history byte per generated token.
+ *   [KVE-lease]  "KV-cache engineering", section "Staging layers under a lease".
+ *   [SWS-queues] "Staging without a stall", section "Two copy queues and
+ *                device-side ordering": dedicated H2D and D2H queues; compute
+ *                waits on an event recorded after the history copy; write-back
+ *                waits on an event recorded after attention; the host never
+ *                blocks on the hot path.
+ *   [SWS-lease]  "Staging without a stall", section "Leases instead of
+ *                buffers": a buffer is reused only after the previous
+ *                attention and write-back that read it; only changed rows go
+ *                back to the pinned host rows; a different host owner is
+ *                refused; any failure quarantines the transport; the
+ *                destructor never waits.
+ *   [SWS-admit]  "Staging without a stall", section "Admission that does
+ *                arithmetic": one explicit device allocation, sink page plus
+ *                newest pages kept hot.
+ *   [GMM-host]   "GPU memory management", section "A host pool that explains
+ *                its own size": a history is, per layer, a segment of
+ *                context length x 4,096 bytes.
+ *
+ * Conventions for every entry point:
+ *   - All memory is allocated and owned by the caller.  The library keeps raw
+ *     pointers only for the lifetime the call documents and never frees them.
+ *   - Streams are the caller's.  Kernels and copies are enqueued
+ *     asynchronously; no entry point synchronises the host except
+ *     kv_arena_drain.
+ *   - Return value: PA_OK (0) or a negative PA_ERR_* code; a thread-local
+ *     message is available from kv_last_error().  No C++ exception crosses
+ *     the ABI.
+ *   - Layouts are dense row-major in the order the brackets list.
+ *
+ * Data layout (the "pool"): a page is PA_PAGE_TOKENS consecutive token rows;
+ * a row is [K of kv heads 0..Hkv-1 | V of kv heads 0..Hkv-1], head_dim bf16
+ * values per head, so row_bytes = 4 * Hkv * head_dim (4,096 at Hkv = 4,
+ * head_dim = 256, as in [GMM-host]).  Token j of a request lives in row
+ * j % PA_PAGE_TOKENS of physical page page_table[request][j / PA_PAGE_TOKENS].
+ * Query head h attends with kv head h / (Hq / Hkv).
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PA_PAGE_TOKENS 64
+
+#define PA_OK                0
+#define PA_ERR_INVALID      -1  /* bad argument (null, size, range, alignment) */
+#define PA_ERR_CUDA         -2  /* a CUDA call failed; arena calls then quarantine */
+#define PA_ERR_QUARANTINED  -3  /* arena is quarantined after an earlier failure */
+#define PA_ERR_ORDER        -4  /* slot busy or call out of order */
+#define PA_ERR_OWNER        -5  /* write-back owner differs from the staged owner */
+#define PA_ERR_UNSUPPORTED  -6  /* geometry not built into this library */
+
+/* Bits OR-ed into the int32 status word at byte 0 of the decode workspace
+ * (and of the optional status word of kv_append_rows) by device code. */
+#define PA_STATUS_BAD_PAGE   1  /* a page id outside [0, pool_pages): tile output is NaN */
+#define PA_STATUS_TIMEOUT    2  /* a bounded device wait gave up: outputs are invalid */
+#define PA_STATUS_BAD_ROW    4  /* kv_append_rows: position or page outside the table/pool */
+
+/* Thread-local message for the last failing call on this thread ("" if none). */
+const char* kv_last_error(void);
+
+/* Library build string (compiler, target architecture). */
+const char* pa_version(void);
+
+/* ------------------------------------------------------------------------ */
+/* Decode attention with per-tile LSE  ([KVE-exact], [KVE-bus])             */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes paged_decode_attn_lse / paged_decode_attn_lse_cuda_core
+ * need for B requests x T tiles of this geometry (an upper bound that does not
+ * depend on tile contents).  Returns 0 for an unsupported geometry. */
+size_t paged_decode_attn_lse_workspace_bytes(int B, int T, int n_q_heads,
+                                             int n_kv_heads, int head_dim);
+
+/* For every request b and tile t = [tiles[b][t][0], tiles[b][t][1]) of its
+ * logical token history, and every query head h:
+ *     s_j        = scale * <q[b][h], K_j of kv head h / G>,   j in the tile
+ *     out[b][t][h] = sum_j exp(s_j - m) V_j / sum_j exp(s_j - m)   (FP32)
+ *     lse[b][t][h] = m + ln sum_j exp(s_j - m)                      (FP32)
+ * with m = max_j s_j.  An empty tile gives out 0 and lse -inf.
+ *
+ *   q          device bf16 [B][n_q_heads][head_dim], 16-byte aligned.
+ *   pool       device bf16 pages (layout above), 16-byte aligned; its row
+ *              stride 4*Hkv*head_dim bytes must be a multiple of 16.
+ *   pool_pages number of pages addressable from pool; a page id outside
+ *              [0, pool_pages) is never read: the tile's output becomes NaN and
+ *              PA_STATUS_BAD_PAGE is set in the workspace status word.
+ *   page_table device int32 [B][max_pages].
+ *   tiles      HOST int32 [B][T][2]; 0 <= start <= end <= max_pages*64 is
+ *              checked (PA_ERR_INVALID).  Tiles may overlap and need not be
+ *              page aligned; rows outside a tile are masked, whatever they hold.
+ *   out, lse   device fp32 [B][T][n_q_heads][head_dim] and [B][T][n_q_heads].
+ *   workspace  device buffer of at least the bytes the query above returns,
+ *              256-byte aligned, ZERO-FILLED before its first use; every call
+ *              leaves it ready for the next (counters return to zero).  Byte 0
+ *              holds the int32 status word (PA_STATUS_* bits, sticky until the
+ *              caller clears it).  Calls that share a workspace must be ordered
+ *              on one stream.
+ * Supported: head_dim 256, n_q_heads / n_kv_heads in 1..8, n_kv_heads >= 1.
+ * Results depend only on the logical tiles and the device's SM count, not on
+ * physical page placement: two calls that differ only in where the pages sit
+ * return bit-identical outputs.  Tensor-core (mma.sync bf16) variant. */
+int paged_decode_attn_lse(const void* q, const void* pool, int64_t pool_pages,
+                          const int32_t* page_table, int max_pages,
+                          const int32_t* tiles, int B, int T,
+                          int n_q_heads, int n_kv_heads, int head_dim,
+                          float scale, float* out, float* lse,
+                          void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream);
+
+/* Same contract, evaluated with FP32 CUDA-core FMAs instead of tensor cores
+ * (kept as the measured alternative). */
+int paged_decode_attn_lse_cuda_core(const void* q, const void* pool, int64_t pool_pages,
+                                    const int32_t* page_table, int max_pages,
+                                    const int32_t* tiles, int B, int T,
+                                    int n_q_heads, int n_kv_heads, int head_dim,
+                                    float scale, float* out, float* lse,
+                                    void* workspace, size_t workspace_bytes,
+                                    cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* FP32 LSE merge  ([KVE-exact])                                            */
+/* ------------------------------------------------------------------------ */
+
+/* For every request b, head h over its partials i in [part_offsets[b],
+ * part_offsets[b+1]), in increasing i:
+ *     M = max_i lse_i;  w_i = exp(lse_i - M);
+ *     out = sum_i w_i out_i / sum_i w_i;  lse = M + ln sum_i w_i.
+ * No partials, or all lse_i = -inf: out 0, lse -inf.  A NaN lse_i gives NaN.
+ * A single partial is returned bit for bit.
+ *   out_parts    device fp32 [n_parts][H][D];  lse_parts device fp32 [n_parts][H]
+ *   part_offsets device int32 [B+1], non-decreasing, part_offsets[0] = 0.
+ *   out, lse     device fp32 [B][H][D], [B][H].
+ * D must be a multiple of 4 and the fp32 arrays 16-byte aligned. */
+int lse_merge(const float* out_parts, const float* lse_parts,
+              const int32_t* part_offsets, int B, int H, int D,
+              float* out, float* lse, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Device tail write: the new token's row into its page  ([SWS-lease])      */
+/* ------------------------------------------------------------------------ */
+
+/* For b < B: copy rows[b] (row_bytes bytes) to the pool row of token
+ * positions[b] of request b, i.e. page page_table[b][positions[b] / 64],
+ * row positions[b] % 64.  An out-of-range position or page id skips the row
+ * and ORs PA_STATUS_BAD_ROW into *status (if status is not NULL).
+ *   pool device; rows device [B][row_bytes]; positions device int32 [B];
+ *   row_bytes a multiple of 16; status device int32 or NULL. */
+int kv_append_rows(void* pool, int64_t pool_pages, const int32_t* page_table,
+                   int max_pages, const int32_t* positions, const void* rows,
+                   int B, int row_bytes, int32_t* status, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ */
+/* Staging arena  ([KVE-bus], [KVE-lease], [SWS-queues], [SWS-lease])       */
+/* ------------------------------------------------------------------------ */
+
+typedef struct kv_arena kv_arena;
+
+#define PA_ARENA_RECORD_ONLY 1u  /* flags: log every CUDA submission instead of
+                                    making it (host-side tests; no GPU needed) */
+
+typedef struct {
+    void*        device_base;     /* caller-owned device memory (256-B aligned)   */
+    uint64_t     device_bytes;    /* explicit size, never inferred  ([SWS-admit]) */
+    int          row_bytes;       /* bytes per token row                           */
+    int          page_tokens;     /* must equal PA_PAGE_TOKENS                     */
+    int          n_slots;         /* staging slots (>= 1; 2 lets copy overlap)     */
+    int64_t      slot_first_page; /* page id, relative to device_base, of slot 0   */
+    int64_t      slot_pages;      /* pages per slot; slot s starts at
+                                     slot_first_page + s * slot_pages              */
+    int32_t*     page_tables;     /* device int32 [n_slots][max_requests][max_pages],
+                                     caller-owned; one table per slot              */
+    int          max_requests;
+    int          max_pages;
+    cudaStream_t compute_stream;  /* attention runs here                           */
+    cudaStream_t h2d_stream;      /* history copies                                */
+    cudaStream_t d2h_stream;      /* tail write-back                               */
+    uint32_t     flags;           /* PA_ARENA_* */
+} kv_arena_desc;
+
+/* A run of consecutive logical pages of one request.  host_rows != NULL: a
+ * staged run, n_rows rows (<= n_pages * page_tokens) are copied from pinned
+ * host memory into the slot.  host_rows == NULL: a resident run whose pages
+ * already sit in the arena at resident_page, resident_page + 1, ... */
+typedef struct {
+    int32_t     logical_page;
+    int32_t     n_pages;
+    int64_t     n_rows;
+    const void* host_rows;
+    int64_t     resident_page;
+} kv_page_run;
+
+typedef struct {
+    int32_t            request;  /* row of the slot's page table               */
+    int32_t            n_runs;
+    const kv_page_run* runs;
+    uint64_t           owner;    /* host owner id the write-back must present  */
+} kv_stage_req;
+
+typedef struct {
+    int32_t  request;   /* request as staged                                   */
+    int32_t  pad_;
+    int64_t  position;  /* token row to write back (its page must be staged or
+                           resident in the layer's stage)                       */
+    void*    host_row;  /* pinned host destination of row_bytes bytes           */
+    uint64_t owner;     /* must equal the owner given to kv_stage_layer (else
+                           PA_ERR_OWNER)                                        */
+} kv_tail_req;
+
+typedef struct {
+    uint64_t stage_generation;  /* stages begun so far; strictly increasing     */
+    uint64_t staged_bytes;      /* bytes enqueued host->device                   */
+    uint64_t written_back_bytes;/* bytes enqueued device->host                   */
+    uint64_t slot_reuses;       /* stages that had to wait on a slot's readers   */
+    int32_t  quarantined;       /* 1 after any failure                           */
+    int32_t  n_slots;
+} kv_arena_stats;
+
+/* Create an arena over caller memory.  Creates one copy, attention and
+ * write-back event per slot.  Fails with PA_ERR_INVALID if the slots do not
+ * fit in device_bytes. */
+int kv_arena_create(const kv_arena_desc* desc, kv_arena** out);
+
+/* Release the arena's events and bookkeeping.  Never waits, submits or drains
+ * ([SWS-lease]); call kv_arena_drain first if work may still be in flight. */
+int kv_arena_destroy(kv_arena* arena);
+
+/* The one host-synchronising call: waits for the H2D, D2H and compute streams.
+ * Returns PA_ERR_CUDA if completion cannot be established (the arena then stays
+ * quarantined and keeps every buffer). */
+int kv_arena_drain(kv_arena* arena);
+
+/* Stage one layer: picks the next slot (round robin), makes the H2D stream
+ * wait on that slot's previous attention and write-back events, enqueues one
+ * H2D copy per staged run, writes the slot's page-table rows for every run
+ * (staged runs get consecutive slot pages in request/run order), records the
+ * slot's copy event and makes the compute stream wait on it.  PA_ERR_ORDER if
+ * the slot's previous stage was never marked attention-done.
+ *   *slot_out        the slot used; *page_table_out its device page table
+ *                    ([max_requests][max_pages]) to pass to the attention. */
+int kv_stage_layer(kv_arena* arena, int layer, const kv_stage_req* reqs,
+                   int n_reqs, int* slot_out, const int32_t** page_table_out);
+
+/* Record the layer's attention-done event on the compute stream; call after
+ * the last kernel that reads the layer's slot. */
+int kv_mark_attention_done(kv_arena* arena, int layer);
+
+/* Tail write-back: the D2H stream waits on the layer's attention event, then
+ * copies each requested row (row_bytes) from the arena to its pinned host row,
+ * and records the slot's write-back event.  Refuses (PA_ERR_OWNER, nothing
+ * enqueued) an owner other than the one the layer was staged with. */
+int kv_writeback_tail(kv_arena* arena, int layer, const kv_tail_req* reqs,
+                      int n_reqs);
+
+/* Counters of the arena. */
+int kv_arena_get_stats(const kv_arena* arena, kv_arena_stats* out);
+
+/* Host-side test hooks.  kv_arena_fail_after: the n-th CUDA submission from
+ * now (0 = the next) reports failure without being made, as a failing driver
+ * call would; the arena then quarantines.  kv_arena_call_log: copies the
+ * record of submissions made under PA_ARENA_RECORD_ONLY (one per line) into
+ * buf, returns the full length. */
+int kv_arena_fail_after(kv_arena* arena, int64_t n);
+size_t kv_arena_call_log(const kv_arena* arena, char* buf, size_t buf_bytes);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -1,0 +1,347 @@
+"""ctypes binding of libpagedattn (argument marshalling only).
+
+Every function here checks shapes, dtypes and devices of torch tensors, takes
+their raw pointers and calls the C-ABI entry point of the same name; all work
+runs in the library's CUDA kernels and copies.  If the shared library is
+missing, importing this module raises: there is no fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpagedattn.so")
+
+PA_OK = 0
+PA_ERR_INVALID = -1
+PA_ERR_CUDA = -2
+PA_ERR_QUARANTINED = -3
+PA_ERR_ORDER = -4
+PA_ERR_OWNER = -5
+PA_ERR_UNSUPPORTED = -6
+PA_STATUS_BAD_PAGE = 1
+PA_STATUS_TIMEOUT = 2
+PA_STATUS_BAD_ROW = 4
+PA_ARENA_RECORD_ONLY = 1
+PAGE_TOKENS = 64
+
+# Every symbol pagedattn.h declares.
+EXPORTED = [
+    "kv_last_error", "pa_version",
+    "paged_decode_attn_lse_workspace_bytes", "paged_decode_attn_lse",
+    "paged_decode_attn_lse_cuda_core", "lse_merge", "kv_append_rows",
+    "kv_arena_create", "kv_arena_destroy", "kv_arena_drain", "kv_stage_layer",
+    "kv_mark_attention_done", "kv_writeback_tail", "kv_arena_get_stats",
+    "kv_arena_fail_after", "kv_arena_call_log",
+]
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, code: int, message: str):
+        super().__init__(f"[{code}] {message}")
+        self.code = code
+
+
+class KvArenaDesc(ctypes.Structure):
+    _fields_ = [
+        ("device_base", ctypes.c_void_p),
+        ("device_bytes", ctypes.c_uint64),
+        ("row_bytes", ctypes.c_int),
+        ("page_tokens", ctypes.c_int),
+        ("n_slots", ctypes.c_int),
+        ("slot_first_page", ctypes.c_int64),
+        ("slot_pages", ctypes.c_int64),
+        ("page_tables", ctypes.c_void_p),
+        ("max_requests", ctypes.c_int),
+        ("max_pages", ctypes.c_int),
+        ("compute_stream", ctypes.c_void_p),
+        ("h2d_stream", ctypes.c_void_p),
+        ("d2h_stream", ctypes.c_void_p),
+        ("flags", ctypes.c_uint32),
+    ]
+
+
+class KvPageRun(ctypes.Structure):
+    _fields_ = [
+        ("logical_page", ctypes.c_int32),
+        ("n_pages", ctypes.c_int32),
+        ("n_rows", ctypes.c_int64),
+        ("host_rows", ctypes.c_void_p),
+        ("resident_page", ctypes.c_int64),
+    ]
+
+
+class KvStageReq(ctypes.Structure):
+    _fields_ = [
+        ("request", ctypes.c_int32),
+        ("n_runs", ctypes.c_int32),
+        ("runs", ctypes.POINTER(KvPageRun)),
+        ("owner", ctypes.c_uint64),
+    ]
+
+
+class KvTailReq(ctypes.Structure):
+    _fields_ = [
+        ("request", ctypes.c_int32),
+        ("pad_", ctypes.c_int32),
+        ("position", ctypes.c_int64),
+        ("host_row", ctypes.c_void_p),
+        ("owner", ctypes.c_uint64),
+    ]
+
+
+class KvArenaStats(ctypes.Structure):
+    _fields_ = [
+        ("stage_generation", ctypes.c_uint64),
+        ("staged_bytes", ctypes.c_uint64),
+        ("written_back_bytes", ctypes.c_uint64),
+        ("slot_reuses", ctypes.c_uint64),
+        ("quarantined", ctypes.c_int32),
+        ("n_slots", ctypes.c_int32),
+    ]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            f"{LIB_PATH} is missing: build it with "
+            "`python -m paged_decode_attention_attn_gb300.build` (no CPU fallback exists)")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, i64, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t
+    lib.kv_last_error.restype = ctypes.c_char_p
+    lib.kv_last_error.argtypes = []
+    lib.pa_version.restype = ctypes.c_char_p
+    lib.pa_version.argtypes = []
+    lib.paged_decode_attn_lse_workspace_bytes.restype = sz
+    lib.paged_decode_attn_lse_workspace_bytes.argtypes = [i32] * 5
+    dec = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
+    for name in ("paged_decode_attn_lse", "paged_decode_attn_lse_cuda_core"):
+        getattr(lib, name).restype = i32
+        getattr(lib, name).argtypes = dec
+    lib.lse_merge.restype = i32
+    lib.lse_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
+    lib.kv_append_rows.restype = i32
+    lib.kv_append_rows.argtypes = [vp, i64, vp, i32, vp, vp, i32, i32, vp, vp]
+    lib.kv_arena_create.restype = i32
+    lib.kv_arena_create.argtypes = [ctypes.POINTER(KvArenaDesc), ctypes.POINTER(vp)]
+    for name in ("kv_arena_destroy", "kv_arena_drain"):
+        getattr(lib, name).restype = i32
+        getattr(lib, name).argtypes = [vp]
+    lib.kv_stage_layer.restype = i32
+    lib.kv_stage_layer.argtypes = [vp, i32, ctypes.POINTER(KvStageReq), i32,
+                                   ctypes.POINTER(i32), ctypes.POINTER(vp)]
+    lib.kv_mark_attention_done.restype = i32
+    lib.kv_mark_attention_done.argtypes = [vp, i32]
+    lib.kv_writeback_tail.restype = i32
+    lib.kv_writeback_tail.argtypes = [vp, i32, ctypes.POINTER(KvTailReq), i32]
+    lib.kv_arena_get_stats.restype = i32
+    lib.kv_arena_get_stats.argtypes = [vp, ctypes.POINTER(KvArenaStats)]
+    lib.kv_arena_fail_after.restype = i32
+    lib.kv_arena_fail_after.argtypes = [vp, i64]
+    lib.kv_arena_call_log.restype = sz
+    lib.kv_arena_call_log.argtypes = [vp, ctypes.c_char_p, sz]
+    return lib
+
+
+lib = _load()
+
+
+def last_error() -> str:
+    return lib.kv_last_error().decode()
+
+
+def _check(rc: int):
+    if rc != PA_OK:
+        raise PagedAttnError(rc, last_error())
+    return rc
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream)
+
+
+def _dev(t: torch.Tensor, dtype, name: str, contiguous: bool = True):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _host_tiles(tiles) -> ctypes.Array:
+    import numpy as np
+    arr = np.ascontiguousarray(np.asarray(tiles, dtype=np.int32))
+    return arr, arr.ctypes.data
+
+
+def workspace_bytes(B: int, T: int, n_q_heads: int, n_kv_heads: int, head_dim: int) -> int:
+    return int(lib.paged_decode_attn_lse_workspace_bytes(B, T, n_q_heads, n_kv_heads, head_dim))
+
+
+def alloc_workspace(B, T, n_q_heads, n_kv_heads, head_dim, device="cuda") -> torch.Tensor:
+    """Zero-filled workspace of the size the library asks for (256-B aligned)."""
+    n = workspace_bytes(B, T, n_q_heads, n_kv_heads, head_dim)
+    if n == 0:
+        raise PagedAttnError(PA_ERR_UNSUPPORTED, "geometry not supported")
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def paged_decode_attn_lse(q, pool, page_table, tiles, scale, out, lse, workspace,
+                          stream=None, cuda_core=False, pool_pages=None):
+    """q bf16 [B][Hq][D]; pool bf16 [pages][64][2*Hkv*D] (or any view whose
+    storage starts at the first page); page_table int32 [B][max_pages];
+    tiles host int32 [B][T][2]; out fp32 [B][T][Hq][D]; lse fp32 [B][T][Hq]."""
+    B, Hq, D = q.shape
+    row_elems = pool.shape[-1]
+    n_kv = row_elems // (2 * D)
+    arr, tiles_ptr = _host_tiles(tiles)
+    T = arr.shape[1]
+    if arr.shape[0] != B:
+        raise ValueError("tiles must be [B][T][2]")
+    if pool_pages is None:
+        pool_pages = pool.numel() // (PAGE_TOKENS * row_elems)
+    fn = lib.paged_decode_attn_lse_cuda_core if cuda_core else lib.paged_decode_attn_lse
+    _check(fn(_dev(q, torch.bfloat16, "q"), _dev(pool, torch.bfloat16, "pool", False),
+              int(pool_pages), _dev(page_table, torch.int32, "page_table"),
+              int(page_table.shape[1]), tiles_ptr, B, T, Hq, n_kv, D, float(scale),
+              _dev(out, torch.float32, "out"), _dev(lse, torch.float32, "lse"),
+              _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
+              _stream_handle(stream)))
+
+
+def lse_merge(out_parts, lse_parts, part_offsets, out, lse, stream=None):
+    """out_parts fp32 [P][H][D]; lse_parts fp32 [P][H]; part_offsets int32 [B+1]
+    (device); out fp32 [B][H][D]; lse fp32 [B][H]."""
+    B = part_offsets.shape[0] - 1
+    H, D = out.shape[-2], out.shape[-1]
+    _check(lib.lse_merge(_dev(out_parts, torch.float32, "out_parts"),
+                         _dev(lse_parts, torch.float32, "lse_parts"),
+                         _dev(part_offsets, torch.int32, "part_offsets"), B, H, D,
+                         _dev(out, torch.float32, "out"), _dev(lse, torch.float32, "lse"),
+                         _stream_handle(stream)))
+
+
+def kv_append_rows(pool, page_table, positions, rows, status=None, stream=None,
+                   pool_pages=None):
+    """Write rows bf16 [B][row_elems] at token positions int32 [B] of each
+    request's pages (device tail write before attention)."""
+    B, row_elems = rows.shape
+    if pool_pages is None:
+        pool_pages = pool.numel() // (PAGE_TOKENS * row_elems)
+    _check(lib.kv_append_rows(_dev(pool, torch.bfloat16, "pool", False), int(pool_pages),
+                              _dev(page_table, torch.int32, "page_table"),
+                              int(page_table.shape[1]), _dev(positions, torch.int32, "positions"),
+                              _dev(rows, torch.bfloat16, "rows"), B, row_elems * 2,
+                              None if status is None else _dev(status, torch.int32, "status"),
+                              _stream_handle(stream)))
+
+
+class Arena:
+    """Owner of a kv_arena handle over caller-allocated device memory."""
+
+    def __init__(self, device_base: int, device_bytes: int, row_bytes: int, n_slots: int,
+                 slot_first_page: int, slot_pages: int, page_tables: int, max_requests: int,
+                 max_pages: int, compute_stream=None, h2d_stream=None, d2h_stream=None,
+                 record_only: bool = False):
+        d = KvArenaDesc()
+        d.device_base = device_base
+        d.device_bytes = device_bytes
+        d.row_bytes = row_bytes
+        d.page_tokens = PAGE_TOKENS
+        d.n_slots = n_slots
+        d.slot_first_page = slot_first_page
+        d.slot_pages = slot_pages
+        d.page_tables = page_tables
+        d.max_requests = max_requests
+        d.max_pages = max_pages
+        d.compute_stream = self._h(compute_stream)
+        d.h2d_stream = self._h(h2d_stream)
+        d.d2h_stream = self._h(d2h_stream)
+        d.flags = PA_ARENA_RECORD_ONLY if record_only else 0
+        self._desc = d
+        h = ctypes.c_void_p()
+        _check(lib.kv_arena_create(ctypes.byref(d), ctypes.byref(h)))
+        self.handle = h
+        self._keep = []
+
+    @staticmethod
+    def _h(s):
+        if s is None:
+            return None
+        if isinstance(s, int):
+            return s
+        return int(s.cuda_stream)
+
+    def stage_layer(self, layer: int, requests):
+        """requests: list of (request, owner, [runs]); a run is a dict with
+        logical_page, n_pages and either host_rows (address) + n_rows, or
+        resident_page.  Returns (slot, page_table_address)."""
+        reqs = (KvStageReq * len(requests))()
+        keep = []
+        for i, (request, owner, runs) in enumerate(requests):
+            arr = (KvPageRun * max(1, len(runs)))()
+            for k, r in enumerate(runs):
+                arr[k].logical_page = r["logical_page"]
+                arr[k].n_pages = r["n_pages"]
+                arr[k].n_rows = r.get("n_rows", 0)
+                arr[k].host_rows = r.get("host_rows")
+                arr[k].resident_page = r.get("resident_page", 0)
+            keep.append(arr)
+            reqs[i].request = request
+            reqs[i].n_runs = len(runs)
+            reqs[i].runs = ctypes.cast(arr, ctypes.POINTER(KvPageRun))
+            reqs[i].owner = owner
+        slot = ctypes.c_int(-1)
+        table = ctypes.c_void_p()
+        _check(lib.kv_stage_layer(self.handle, layer, reqs, len(requests), ctypes.byref(slot),
+                                  ctypes.byref(table)))
+        return slot.value, table.value
+
+    def mark_attention_done(self, layer: int):
+        _check(lib.kv_mark_attention_done(self.handle, layer))
+
+    def writeback_tail(self, layer: int, tails):
+        """tails: list of (request, position, host_row_address, owner)."""
+        arr = (KvTailReq * max(1, len(tails)))()
+        for i, (request, position, host_row, owner) in enumerate(tails):
+            arr[i].request = request
+            arr[i].position = position
+            arr[i].host_row = host_row
+            arr[i].owner = owner
+        _check(lib.kv_writeback_tail(self.handle, layer, arr, len(tails)))
+
+    def drain(self):
+        _check(lib.kv_arena_drain(self.handle))
+
+    def stats(self) -> KvArenaStats:
+        s = KvArenaStats()
+        _check(lib.kv_arena_get_stats(self.handle, ctypes.byref(s)))
+        return s
+
+    def fail_after(self, n: int):
+        _check(lib.kv_arena_fail_after(self.handle, n))
+
+    def call_log(self) -> list:
+        n = lib.kv_arena_call_log(self.handle, None, 0)
+        buf = ctypes.create_string_buffer(n + 1)
+        lib.kv_arena_call_log(self.handle, buf, n + 1)
+        return [line for line in buf.value.decode().split("\n") if line]
+
+    def close(self):
+        if self.handle:
+            lib.kv_arena_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,495 @@
+// Staging arena: pinned-host-owned KV history staged per layer into bounded
+// device slots, ordered against attention and tail write-back by device events.
+//
+// Sources ("Staging without a stall", sections "Two copy queues and
+// device-side ordering" and "Leases instead of buffers"; "KV-cache
+// engineering", sections "Costing the bus before changing anything" and
+// "Staging layers under a lease"):
+//   * pinned host memory owns the history; the device holds a bounded set of
+//     slots inside one explicitly sized allocation;
+//   * the history copy runs on its own H2D stream and the compute stream waits
+//     on an event recorded after it; the write-back runs on its own D2H stream
+//     after an event recorded after attention; the host never blocks;
+//   * a slot is reused only after the attention and the write-back that read
+//     it: the next copy into the slot first waits on both events;
+//   * only the new token's row goes back, and only to the owner the stage was
+//     made for;
+//   * any failure quarantines the arena; only a drain that establishes
+//     completion releases it; destroy never waits, submits or drains.
+#include <cuda_runtime.h>
+
+#include <cinttypes>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <string>
+#include <vector>
+
+#include "common.h"
+
+namespace pa {
+namespace arena {
+
+constexpr int kMaxRunsPerLaunch = 128;
+
+struct TableRun {
+  int32_t request;
+  int32_t logical_page;
+  int32_t n_pages;
+  int32_t pad;
+  long long first_page;
+};
+
+struct TableParams {
+  int32_t* table;
+  int max_pages;
+  int n_runs;
+  TableRun runs[kMaxRunsPerLaunch];
+};
+
+// Writes table[request][logical_page + i] = first_page + i for every run.
+__global__ void fill_page_table_kernel(const __grid_constant__ TableParams p) {
+  for (int r = blockIdx.x; r < p.n_runs; r += gridDim.x) {
+    const TableRun run = p.runs[r];
+    int32_t* row = p.table + (size_t)run.request * p.max_pages + run.logical_page;
+    for (int i = threadIdx.x; i < run.n_pages; i += blockDim.x)
+      row[i] = static_cast<int32_t>(run.first_page + i);
+  }
+}
+
+enum SlotState { kFree = 0, kStaged = 1, kAttended = 2 };
+
+struct ReqRecord {
+  int32_t request;
+  uint64_t owner;
+  std::vector<kv_page_run> runs;
+  std::vector<int64_t> first_page;  // device page of each run's first page
+};
+
+struct Slot {
+  SlotState state = kFree;
+  int layer = -1;
+  uint64_t generation = 0;
+  bool written_back = false;
+  std::vector<ReqRecord> reqs;
+};
+
+}  // namespace arena
+}  // namespace pa
+
+struct kv_arena {
+  kv_arena_desc d{};
+  bool record_only = false;
+  bool quarantined = false;
+  int64_t fail_after = -1;
+  std::string log;
+  std::vector<cudaEvent_t> ev_copy, ev_attn, ev_wb;
+  std::vector<pa::arena::Slot> slots;
+  std::map<int, int> layer_slot;
+  uint64_t generation = 0;
+  uint64_t staged_bytes = 0;
+  uint64_t written_back_bytes = 0;
+  uint64_t slot_reuses = 0;
+  int64_t page_bytes = 0;
+  int64_t arena_pages = 0;
+};
+
+namespace pa {
+namespace arena {
+
+namespace {
+
+int quarantine(kv_arena* a, const char* what, cudaError_t e) {
+  a->quarantined = true;
+  return fail(PA_ERR_CUDA, "%s failed (%s); arena quarantined", what,
+              e == cudaSuccess ? "injected failure" : cudaGetErrorString(e));
+}
+
+// Gate every submission: honours the injected-failure countdown.
+bool injected_failure(kv_arena* a) {
+  if (a->fail_after < 0) return false;
+  if (a->fail_after == 0) {
+    a->fail_after = -1;
+    return true;
+  }
+  --a->fail_after;
+  return false;
+}
+
+void logf_(kv_arena* a, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+void logf_(kv_arena* a, const char* fmt, ...) {
+  char buf[256];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  a->log += buf;
+  a->log += '\n';
+}
+
+const char* stream_name(kv_arena* a, cudaStream_t s) {
+  if (s == a->d.h2d_stream) return "h2d";
+  if (s == a->d.d2h_stream) return "d2h";
+  if (s == a->d.compute_stream) return "compute";
+  return "?";
+}
+
+int op_wait(kv_arena* a, cudaStream_t s, const char* ev_kind, int slot, cudaEvent_t ev) {
+  if (injected_failure(a)) return quarantine(a, "cudaStreamWaitEvent", cudaSuccess);
+  if (a->record_only) {
+    logf_(a, "%s wait %s[%d]", stream_name(a, s), ev_kind, slot);
+    return PA_OK;
+  }
+  const cudaError_t e = cudaStreamWaitEvent(s, ev, 0);
+  return e == cudaSuccess ? PA_OK : quarantine(a, "cudaStreamWaitEvent", e);
+}
+
+int op_record(kv_arena* a, cudaStream_t s, const char* ev_kind, int slot, cudaEvent_t ev) {
+  if (injected_failure(a)) return quarantine(a, "cudaEventRecord", cudaSuccess);
+  if (a->record_only) {
+    logf_(a, "%s record %s[%d]", stream_name(a, s), ev_kind, slot);
+    return PA_OK;
+  }
+  const cudaError_t e = cudaEventRecord(ev, s);
+  return e == cudaSuccess ? PA_OK : quarantine(a, "cudaEventRecord", e);
+}
+
+int op_copy(kv_arena* a, cudaStream_t s, void* dst, const void* src, size_t bytes,
+            cudaMemcpyKind kind, long long dev_page, long long row) {
+  if (injected_failure(a)) return quarantine(a, "cudaMemcpyAsync", cudaSuccess);
+  if (a->record_only) {
+    logf_(a, "%s copy %s bytes=%zu page=%lld row=%lld", stream_name(a, s),
+          kind == cudaMemcpyHostToDevice ? "h2d" : "d2h", bytes, dev_page, row);
+    return PA_OK;
+  }
+  const cudaError_t e = cudaMemcpyAsync(dst, src, bytes, kind, s);
+  return e == cudaSuccess ? PA_OK : quarantine(a, "cudaMemcpyAsync", e);
+}
+
+int op_table(kv_arena* a, cudaStream_t s, int slot, const TableParams& p) {
+  if (injected_failure(a)) return quarantine(a, "page-table kernel launch", cudaSuccess);
+  if (a->record_only) {
+    std::string line;
+    char buf[96];
+    snprintf(buf, sizeof(buf), "%s table slot=%d runs=%d", stream_name(a, s), slot, p.n_runs);
+    line = buf;
+    for (int i = 0; i < p.n_runs; ++i) {
+      snprintf(buf, sizeof(buf), " %d:%d+%d->%lld", p.runs[i].request, p.runs[i].logical_page,
+               p.runs[i].n_pages, p.runs[i].first_page);
+      line += buf;
+    }
+    a->log += line;
+    a->log += '\n';
+    return PA_OK;
+  }
+  const int blocks = p.n_runs < 1 ? 1 : p.n_runs;
+  fill_page_table_kernel<<<blocks, 256, 0, s>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : quarantine(a, "page-table kernel launch", e);
+}
+
+}  // namespace
+
+}  // namespace arena
+}  // namespace pa
+
+using pa::fail;
+using namespace pa::arena;
+
+extern "C" int kv_arena_create(const kv_arena_desc* desc, kv_arena** out) {
+  pa::clear_error();
+  PA_REQUIRE(desc && out, "null pointer argument");
+  *out = nullptr;
+  const kv_arena_desc& d = *desc;
+  PA_REQUIRE(d.device_base != nullptr, "device_base is null");
+  PA_REQUIRE(reinterpret_cast<uintptr_t>(d.device_base) % 256 == 0,
+             "device_base must be 256-byte aligned");
+  PA_REQUIRE(d.row_bytes > 0 && d.row_bytes % 16 == 0,
+             "row_bytes (%d) must be a positive multiple of 16", d.row_bytes);
+  PA_REQUIRE(d.page_tokens == PA_PAGE_TOKENS, "page_tokens must be %d", PA_PAGE_TOKENS);
+  PA_REQUIRE(d.n_slots >= 1 && d.n_slots <= 64, "n_slots (%d) must be in 1..64", d.n_slots);
+  PA_REQUIRE(d.slot_pages >= 1 && d.slot_first_page >= 0, "bad slot geometry");
+  PA_REQUIRE(d.page_tables != nullptr && d.max_requests >= 1 && d.max_pages >= 1,
+             "page_tables, max_requests and max_pages are required");
+  const int64_t page_bytes = (int64_t)d.row_bytes * d.page_tokens;
+  const int64_t arena_pages = (int64_t)(d.device_bytes / (uint64_t)page_bytes);
+  PA_REQUIRE(d.slot_first_page + (int64_t)d.n_slots * d.slot_pages <= arena_pages,
+             "slots need %" PRId64 " pages of %" PRId64 " bytes but device_bytes holds %" PRId64,
+             d.slot_first_page + (int64_t)d.n_slots * d.slot_pages, page_bytes, arena_pages);
+  PA_REQUIRE(arena_pages < (1ll << 31), "arena too large for 32-bit page ids");
+
+  kv_arena* a = new kv_arena;
+  a->d = d;
+  a->record_only = (d.flags & PA_ARENA_RECORD_ONLY) != 0;
+  a->page_bytes = page_bytes;
+  a->arena_pages = arena_pages;
+  a->slots.resize(d.n_slots);
+  a->ev_copy.assign(d.n_slots, nullptr);
+  a->ev_attn.assign(d.n_slots, nullptr);
+  a->ev_wb.assign(d.n_slots, nullptr);
+  if (!a->record_only) {
+    for (int s = 0; s < d.n_slots; ++s) {
+      cudaError_t e = cudaEventCreateWithFlags(&a->ev_copy[s], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a->ev_attn[s], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a->ev_wb[s], cudaEventDisableTiming);
+      if (e != cudaSuccess) {
+        kv_arena_destroy(a);
+        return fail(PA_ERR_CUDA, "cudaEventCreateWithFlags failed: %s", cudaGetErrorString(e));
+      }
+    }
+  }
+  *out = a;
+  return PA_OK;
+}
+
+extern "C" int kv_arena_destroy(kv_arena* a) {
+  pa::clear_error();
+  if (!a) return PA_OK;
+  // Never waits: destroying an event with work pending releases it when done.
+  for (auto* v : {&a->ev_copy, &a->ev_attn, &a->ev_wb})
+    for (cudaEvent_t e : *v)
+      if (e) cudaEventDestroy(e);
+  delete a;
+  return PA_OK;
+}
+
+extern "C" int kv_arena_drain(kv_arena* a) {
+  pa::clear_error();
+  PA_REQUIRE(a, "null arena");
+  if (a->record_only) {
+    if (injected_failure(a)) return quarantine(a, "drain", cudaSuccess);
+    logf_(a, "drain");
+  } else {
+    for (cudaStream_t s : {a->d.h2d_stream, a->d.d2h_stream, a->d.compute_stream}) {
+      const cudaError_t e = cudaStreamSynchronize(s);
+      if (e != cudaSuccess) return quarantine(a, "cudaStreamSynchronize", e);
+    }
+  }
+  // Completion is established: every slot is free again.
+  for (auto& s : a->slots) {
+    s.state = kFree;
+    s.written_back = false;
+    s.reqs.clear();
+  }
+  a->layer_slot.clear();
+  a->quarantined = false;
+  return PA_OK;
+}
+
+extern "C" int kv_stage_layer(kv_arena* a, int layer, const kv_stage_req* reqs, int n_reqs,
+                              int* slot_out, const int32_t** page_table_out) {
+  pa::clear_error();
+  PA_REQUIRE(a, "null arena");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  PA_REQUIRE(layer >= 0, "layer must be >= 0");
+  PA_REQUIRE(n_reqs >= 0 && (n_reqs == 0 || reqs), "bad request list");
+  const kv_arena_desc& d = a->d;
+  const int slot = static_cast<int>(a->generation % (uint64_t)d.n_slots);
+  Slot& S = a->slots[slot];
+  if (S.state == kStaged)
+    return fail(PA_ERR_ORDER,
+                "slot %d still holds layer %d, which was never marked attention-done", slot,
+                S.layer);
+
+  // ---- validate everything before submitting anything ----
+  std::vector<char> seen(d.max_requests, 0);
+  int64_t staged_pages = 0;
+  int n_table_runs = 0;
+  for (int i = 0; i < n_reqs; ++i) {
+    const kv_stage_req& r = reqs[i];
+    PA_REQUIRE(r.request >= 0 && r.request < d.max_requests, "request %d outside [0, %d)",
+               r.request, d.max_requests);
+    PA_REQUIRE(!seen[r.request], "request %d staged twice", r.request);
+    seen[r.request] = 1;
+    PA_REQUIRE(r.n_runs >= 0 && (r.n_runs == 0 || r.runs), "request %d: bad run list",
+               r.request);
+    for (int k = 0; k < r.n_runs; ++k) {
+      const kv_page_run& run = r.runs[k];
+      PA_REQUIRE(run.logical_page >= 0 && run.n_pages >= 1 &&
+                     (int64_t)run.logical_page + run.n_pages <= d.max_pages,
+                 "request %d run %d: pages [%d, +%d) outside the table", r.request, k,
+                 run.logical_page, run.n_pages);
+      if (run.host_rows) {
+        PA_REQUIRE(run.n_rows >= 0 && run.n_rows <= (int64_t)run.n_pages * d.page_tokens,
+                   "request %d run %d: %" PRId64 " rows do not fit %d pages", r.request, k,
+                   run.n_rows, run.n_pages);
+        if (!a->record_only) {
+          cudaPointerAttributes attr;
+          const cudaError_t e = cudaPointerGetAttributes(&attr, run.host_rows);
+          PA_REQUIRE(e == cudaSuccess && attr.type == cudaMemoryTypeHost,
+                     "request %d run %d: host rows must be pinned host memory", r.request, k);
+        }
+        staged_pages += run.n_pages;
+      } else {
+        PA_REQUIRE(run.resident_page >= 0 && run.resident_page + run.n_pages <= a->arena_pages,
+                   "request %d run %d: resident pages outside the arena", r.request, k);
+      }
+      ++n_table_runs;
+    }
+  }
+  PA_REQUIRE(staged_pages <= d.slot_pages, "stage needs %" PRId64 " pages, a slot holds %" PRId64,
+             staged_pages, d.slot_pages);
+
+  // ---- submit ----
+  const cudaStream_t h2d = d.h2d_stream;
+  int rc;
+  if (S.state != kFree) {
+    ++a->slot_reuses;
+    if ((rc = op_wait(a, h2d, "attn", slot, a->ev_attn[slot])) != PA_OK) return rc;
+    if (S.written_back && (rc = op_wait(a, h2d, "wb", slot, a->ev_wb[slot])) != PA_OK) return rc;
+  }
+  uint8_t* base = static_cast<uint8_t*>(d.device_base);
+  const int64_t slot_page0 = d.slot_first_page + (int64_t)slot * d.slot_pages;
+  std::vector<ReqRecord> records;
+  records.reserve(n_reqs);
+  std::vector<TableRun> table_runs;
+  table_runs.reserve(n_table_runs);
+  int64_t cursor = 0;
+  for (int i = 0; i < n_reqs; ++i) {
+    const kv_stage_req& r = reqs[i];
+    ReqRecord rec;
+    rec.request = r.request;
+    rec.owner = r.owner;
+    for (int k = 0; k < r.n_runs; ++k) {
+      const kv_page_run& run = r.runs[k];
+      int64_t first;
+      if (run.host_rows) {
+        first = slot_page0 + cursor;
+        cursor += run.n_pages;
+        const size_t bytes = (size_t)run.n_rows * d.row_bytes;
+        if (bytes > 0) {
+          if ((rc = op_copy(a, h2d, base + first * a->page_bytes, run.host_rows, bytes,
+                            cudaMemcpyHostToDevice, first, 0)) != PA_OK)
+            return rc;
+          a->staged_bytes += bytes;
+        }
+      } else {
+        first = run.resident_page;
+      }
+      rec.runs.push_back(run);
+      rec.first_page.push_back(first);
+      table_runs.push_back(TableRun{r.request, run.logical_page, run.n_pages, 0, first});
+    }
+    records.push_back(std::move(rec));
+  }
+  int32_t* table = d.page_tables + (size_t)slot * d.max_requests * d.max_pages;
+  for (size_t r0 = 0; r0 < table_runs.size(); r0 += kMaxRunsPerLaunch) {
+    TableParams tp{};
+    tp.table = table;
+    tp.max_pages = d.max_pages;
+    tp.n_runs = static_cast<int>(std::min<size_t>(kMaxRunsPerLaunch, table_runs.size() - r0));
+    std::memcpy(tp.runs, table_runs.data() + r0, tp.n_runs * sizeof(TableRun));
+    if ((rc = op_table(a, h2d, slot, tp)) != PA_OK) return rc;
+  }
+  if ((rc = op_record(a, h2d, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
+  if ((rc = op_wait(a, d.compute_stream, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
+
+  S.state = kStaged;
+  S.layer = layer;
+  S.generation = ++a->generation;
+  S.written_back = false;
+  S.reqs = std::move(records);
+  a->layer_slot[layer] = slot;
+  if (slot_out) *slot_out = slot;
+  if (page_table_out) *page_table_out = table;
+  return PA_OK;
+}
+
+extern "C" int kv_mark_attention_done(kv_arena* a, int layer) {
+  pa::clear_error();
+  PA_REQUIRE(a, "null arena");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  const auto it = a->layer_slot.find(layer);
+  if (it == a->layer_slot.end()) return fail(PA_ERR_ORDER, "layer %d has no current stage", layer);
+  Slot& S = a->slots[it->second];
+  if (S.layer != layer || S.state != kStaged)
+    return fail(PA_ERR_ORDER, "layer %d is not awaiting attention (slot %d)", layer, it->second);
+  const int rc = op_record(a, a->d.compute_stream, "attn", it->second, a->ev_attn[it->second]);
+  if (rc != PA_OK) return rc;
+  S.state = kAttended;
+  return PA_OK;
+}
+
+extern "C" int kv_writeback_tail(kv_arena* a, int layer, const kv_tail_req* reqs, int n_reqs) {
+  pa::clear_error();
+  PA_REQUIRE(a, "null arena");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  PA_REQUIRE(n_reqs >= 0 && (n_reqs == 0 || reqs), "bad request list");
+  const auto it = a->layer_slot.find(layer);
+  if (it == a->layer_slot.end()) return fail(PA_ERR_ORDER, "layer %d has no current stage", layer);
+  const int slot = it->second;
+  Slot& S = a->slots[slot];
+  if (S.layer != layer || S.state != kAttended)
+    return fail(PA_ERR_ORDER, "write-back of layer %d before its attention was marked done",
+                layer);
+  const kv_arena_desc& d = a->d;
+  std::vector<uint8_t*> src(n_reqs);
+  for (int i = 0; i < n_reqs; ++i) {
+    const kv_tail_req& t = reqs[i];
+    PA_REQUIRE(t.host_row != nullptr, "tail %d: null host row", i);
+    const ReqRecord* rec = nullptr;
+    for (const auto& r : S.reqs)
+      if (r.request == t.request) rec = &r;
+    PA_REQUIRE(rec != nullptr, "tail %d: request %d was not staged for layer %d", i, t.request,
+               layer);
+    if (rec->owner != t.owner)
+      return fail(PA_ERR_OWNER,
+                  "tail %d: owner %" PRIu64 " differs from the owner %" PRIu64
+                  " request %d was staged with",
+                  i, t.owner, rec->owner, t.request);
+    PA_REQUIRE(t.position >= 0, "tail %d: negative position", i);
+    const int64_t lp = t.position / d.page_tokens;
+    int64_t page = -1;
+    for (size_t k = 0; k < rec->runs.size(); ++k) {
+      const kv_page_run& run = rec->runs[k];
+      if (lp >= run.logical_page && lp < (int64_t)run.logical_page + run.n_pages)
+        page = rec->first_page[k] + (lp - run.logical_page);
+    }
+    PA_REQUIRE(page >= 0, "tail %d: position %" PRId64 " is not in a staged or resident run", i,
+               t.position);
+    src[i] = static_cast<uint8_t*>(d.device_base) +
+             (page * d.page_tokens + t.position % d.page_tokens) * (int64_t)d.row_bytes;
+  }
+  int rc;
+  if ((rc = op_wait(a, d.d2h_stream, "attn", slot, a->ev_attn[slot])) != PA_OK) return rc;
+  for (int i = 0; i < n_reqs; ++i) {
+    const int64_t off = src[i] - static_cast<uint8_t*>(d.device_base);
+    if ((rc = op_copy(a, d.d2h_stream, reqs[i].host_row, src[i], d.row_bytes,
+                      cudaMemcpyDeviceToHost, off / a->page_bytes,
+                      (off % a->page_bytes) / d.row_bytes)) != PA_OK)
+      return rc;
+    a->written_back_bytes += d.row_bytes;
+  }
+  if ((rc = op_record(a, d.d2h_stream, "wb", slot, a->ev_wb[slot])) != PA_OK) return rc;
+  S.written_back = true;
+  return PA_OK;
+}
+
+extern "C" int kv_arena_get_stats(const kv_arena* a, kv_arena_stats* out) {
+  pa::clear_error();
+  PA_REQUIRE(a && out, "null pointer argument");
+  out->stage_generation = a->generation;
+  out->staged_bytes = a->staged_bytes;
+  out->written_back_bytes = a->written_back_bytes;
+  out->slot_reuses = a->slot_reuses;
+  out->quarantined = a->quarantined ? 1 : 0;
+  out->n_slots = a->d.n_slots;
+  return PA_OK;
+}
+
+extern "C" int kv_arena_fail_after(kv_arena* a, int64_t n) {
+  pa::clear_error();
+  PA_REQUIRE(a, "null arena");
+  a->fail_after = n;
+  return PA_OK;
+}
+
+extern "C" size_t kv_arena_call_log(const kv_arena* a, char* buf, size_t buf_bytes) {
+  if (!a) return 0;
+  if (buf && buf_bytes) {
+    const size_t n = std::min(buf_bytes - 1, a->log.size());
+    std::memcpy(buf, a->log.data(), n);
+    buf[n] = '\0';
+  }
+  return a->log.size();
+}

@@ -1,0 +1,47 @@
+// Error reporting and small device queries shared by every entry point.
+#include "common.h"
+
+#include <cstdio>
+#include <mutex>
+
+namespace pa {
+
+namespace {
+thread_local char g_message[1024] = "";
+}
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_message, sizeof(g_message), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+void clear_error() { g_message[0] = '\0'; }
+
+int sm_count() {
+  static std::mutex mu;
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return 0;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+}  // namespace pa
+
+extern "C" const char* kv_last_error(void) { return pa::g_message; }
+
+#define PA_STR2(x) #x
+#define PA_STR(x) PA_STR2(x)
+
+extern "C" const char* pa_version(void) {
+  return "libpagedattn 0.1 (sm_103a, CUDA runtime " PA_STR(CUDART_VERSION) ")";
+}

@@ -1,0 +1,905 @@
+// Split-KV paged GQA decode attention with a per-tile log-sum-exp, for sm_103a.
+//
+// What it computes ("KV-cache engineering", section "Exact recent pages,
+// compact older pages"): for every tile of a request's history and every
+// query head, the softmax-normalised output over the tile's keys and the
+// tile's log-sum-exp, so that tiles can later be merged exactly.  The history
+// is read once per call ("Costing the bus before changing anything": the exact
+// path re-reads every byte of history for every generated token), so the
+// kernel is bound by HBM bandwidth and is built around keeping HBM busy:
+//
+//  * Work = (tile, kv head) units, each a run of 64-token pages.  All units'
+//    pages are laid end to end and cut into one contiguous page range per CTA
+//    (persistent grid, one CTA per SM), so every SM streams the same number of
+//    pages whatever the mix of lengths.  A unit that spans several CTAs leaves
+//    one partial (max, sum, unnormalised output) per CTA; the last CTA to
+//    finish merges them in CTA order, so the result does not depend on timing
+//    or on where pages sit physically.
+//  * One producer warp streams pages with TMA: per page the K slice and the V
+//    slice of one kv head (64 rows x 512 B each, row stride 4 KiB) as eight
+//    64x64 boxes with the 128-byte swizzle, into a 3-stage mbarrier ring
+//    (64 KiB per stage).
+//  * Four consumer warps each take 16 tokens of every page.  All G <= 8 query
+//    heads of the GQA group share the page, so the grouped scores are a
+//    16 x 8 x 256 product per warp (tensor-core mma.sync m16n8k16, heads as
+//    rows, bf16 in, fp32 accumulate).  Online softmax runs in the log2 domain
+//    with a lazy rescale (the running reference only moves when the max grows
+//    by more than 2^8).  P enters the PV product as a hi + lo pair of bf16
+//    values packed into the otherwise idle rows 8..15 of the A tile, which
+//    keeps ~16 significant bits of every probability at no extra MMA cost.
+//  * A CUDA-core variant (FP32 FMAs, one lane per 8 dims) runs the same
+//    pipeline; it exists to measure the tensor-core choice against.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace pa {
+namespace decode {
+
+constexpr int kPage = PA_PAGE_TOKENS;                    // tokens per page
+constexpr int kD = 256;                                  // head_dim
+constexpr int kMaxG = 8;                                 // query heads per kv head
+constexpr int kStages = 3;
+constexpr int kConsumerWarps = 4;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kThreads = kConsumers + 32;                // + one producer warp
+constexpr int kBoxCols = 64;                             // 128 B swizzle span
+constexpr int kBoxBytes = kPage * kBoxCols * 2;          // 8 KiB
+constexpr int kHalfBytes = kBoxBytes * (kD / kBoxCols);  // K (or V) slice: 32 KiB
+constexpr int kStageBytes = 2 * kHalfBytes;              // 64 KiB
+constexpr int kXRow = kD + 8;                            // padded exchange row
+constexpr int kXOBytes = kConsumerWarps * kMaxG * kXRow * 4;
+constexpr int kXMLBytes = kConsumerWarps * kMaxG * 2 * 4;
+constexpr int kSmemXO = kStages * kStageBytes;
+constexpr int kSmemXML = kSmemXO + kXOBytes;
+constexpr int kSmemBar = kSmemXML + kXMLBytes;
+constexpr int kSmemMisc = kSmemBar + 2 * kStages * 8;
+constexpr int kSmemUsed = kSmemMisc + 64;
+constexpr int kSmemAlloc = kSmemUsed + 1024;             // slack to align to 1 KiB
+constexpr int kMaxGrid = 1024;
+constexpr int kMaxUnitsLarge = 1024;
+constexpr int kMaxUnitsSmall = 64;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;         // 2 s per wait
+constexpr size_t kStatusBytes = 256;
+constexpr size_t kCounterBytes = 4 * kMaxUnitsLarge;
+constexpr size_t kPartOBytes = size_t(kMaxG) * kD * 4;   // per partial slot
+constexpr size_t kPartMLBytes = size_t(kMaxG) * 2 * 4;
+constexpr float kLn2 = 0.693147180559945309f;
+constexpr float kLog2e = 1.44269504088896341f;
+constexpr float kRescaleThreshold = 8.0f;                // log2 units
+
+static_assert(kSmemAlloc <= 232448, "shared memory budget");
+
+struct Unit {
+  int32_t bt_g;        // (b * T + t) * Hkv + g
+  int32_t tok_start;
+  int32_t tok_end;
+  int32_t page_first;  // flattened index of the unit's first page in this launch
+  int32_t part_base;   // first partial slot (units covered by several CTAs)
+  int32_t n_parts;     // CTAs covering the unit
+};
+
+template <int kMaxUnits>
+struct Params {
+  const __nv_bfloat16* q;
+  const int32_t* page_table;
+  float* out;
+  float* lse;
+  int32_t* status;
+  int32_t* counters;
+  float* part_o;   // [slot][kMaxG][kD]
+  float* part_ml;  // [slot][kMaxG][2]
+  long long pool_pages;
+  long long total_pages;
+  int max_pages;
+  int T;
+  int Hq;
+  int Hkv;
+  int G;
+  int n_units;
+  int grid;
+  float scale_log2;
+  Unit units[kMaxUnits];
+};
+
+__host__ __device__ __forceinline__ int unit_pages(int tok_start, int tok_end) {
+  return tok_end > tok_start ? (tok_end + kPage - 1) / kPage - tok_start / kPage : 0;
+}
+
+// CTA whose page range [k P / grid, (k+1) P / grid) holds flattened page p.
+__host__ __device__ __forceinline__ int cta_of(long long p, long long total, int grid) {
+  return static_cast<int>(((p + 1) * grid - 1) / total);
+}
+
+template <int N>
+__device__ __forceinline__ int first_unit(const Params<N>& p, long long start) {
+  int lo = 0, hi = p.n_units - 1, ans = 0;
+  while (lo <= hi) {
+    const int mid = (lo + hi) >> 1;
+    if (p.units[mid].page_first <= start) {
+      ans = mid;
+      lo = mid + 1;
+    } else {
+      hi = mid - 1;
+    }
+  }
+  return ans;
+}
+
+struct Shared {
+  uint8_t* stages;
+  float* xo;       // [warp][kMaxG][kXRow]
+  float* xml;      // [warp][kMaxG][2]
+  uint32_t full_bar;
+  uint32_t empty_bar;
+  volatile int* poison;  // [kStages]
+  volatile int* abort_flag;
+  volatile int* merge_flag;
+};
+
+__device__ __forceinline__ Shared carve(uint8_t* raw) {
+  Shared s;
+  uint8_t* base = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+  s.stages = base;
+  s.xo = reinterpret_cast<float*>(base + kSmemXO);
+  s.xml = reinterpret_cast<float*>(base + kSmemXML);
+  s.full_bar = ptx::smem_addr(base + kSmemBar);
+  s.empty_bar = s.full_bar + kStages * 8;
+  int* misc = reinterpret_cast<int*>(base + kSmemMisc);
+  s.poison = misc;
+  s.abort_flag = misc + kStages;
+  s.merge_flag = misc + kStages + 1;
+  return s;
+}
+
+// ---------------------------------------------------------------------------
+// Per-warp accumulators of one segment (tensor-core variant).
+// o[n][0..1]: head row (lane/4), dims 8n + 2(lane%4) + {0,1}, from P_hi;
+// o[n][2..3]: the same head and dims, from P_lo.
+// ---------------------------------------------------------------------------
+struct MmaState {
+  float o[kD / 8][4];
+  float m;  // running reference max of this lane's head row (log2 domain)
+  float l;  // this lane's share of the row sum (quad-reduced at the end)
+};
+
+struct FmaState {
+  float o[kMaxG][8];  // head h, dims 8*lane .. 8*lane+7
+  float m[kMaxG];
+  float l[kMaxG];
+};
+
+// ---------------------------------------------------------------------------
+// The kernel.
+// ---------------------------------------------------------------------------
+template <int kMaxUnits, bool kTensorCores>
+__global__ void __launch_bounds__(kThreads, 1)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap,
+                        const __grid_constant__ Params<kMaxUnits> p) {
+  extern __shared__ uint8_t smem_raw[];
+  const Shared sh = carve(smem_raw);
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.G;
+  const int Hkv = p.Hkv;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(sh.full_bar + 8 * s, 1);
+      ptx::mbar_init(sh.empty_bar + 8 * s, kConsumerWarps);
+      sh.poison[s] = 0;
+    }
+    *sh.abort_flag = 0;
+    *sh.merge_flag = 0;
+    ptx::mbar_init_fence();
+  }
+  __syncthreads();
+
+  const long long cta_start = (long long)blockIdx.x * p.total_pages / p.grid;
+  const long long cta_end = (long long)(blockIdx.x + 1) * p.total_pages / p.grid;
+
+  // ======================= producer warp =======================
+  if (warp == kConsumerWarps) {
+    int it = 0;
+    bool ok = true;
+    for (int u = first_unit(p, cta_start); ok && u < p.n_units && p.units[u].page_first < cta_end;
+         ++u) {
+      const Unit U = p.units[u];
+      const int np = unit_pages(U.tok_start, U.tok_end);
+      if (np == 0) continue;
+      const long long pf = U.page_first;
+      const int lo = static_cast<int>(max(cta_start, pf) - pf);
+      const int hi = static_cast<int>(min(cta_end, pf + np) - pf);
+      const int bt = U.bt_g / Hkv;
+      const int g = U.bt_g - bt * Hkv;
+      const int b = bt / p.T;
+      const int32_t* prow = p.page_table + (size_t)b * p.max_pages + U.tok_start / kPage;
+      const int xk = g * kD;
+      const int xv = (Hkv + g) * kD;
+      for (int base = lo; ok && base < hi; base += 32) {
+        const int cnt = min(32, hi - base);
+        const int my_pid = lane < cnt ? __ldg(prow + base + lane) : 0;
+        for (int j = 0; j < cnt; ++j) {
+          const int pid = __shfl_sync(0xffffffffu, my_pid, j);
+          int good = 1;
+          if (lane == 0) {
+            const int s = it % kStages;
+            if (it >= kStages) {
+              good = ptx::mbar_wait_bounded(sh.empty_bar + 8 * s, ((it / kStages) - 1) & 1,
+                                            kWaitLimitNs) ? 1 : 0;
+            }
+            if (good) {
+              const bool bad = pid < 0 || (long long)pid >= p.pool_pages;
+              if (bad) atomicOr(p.status, PA_STATUS_BAD_PAGE);
+              sh.poison[s] = bad ? 1 : 0;
+              const int y = (bad ? 0 : pid) * kPage;
+              const uint32_t full = sh.full_bar + 8 * s;
+              const uint32_t dst = ptx::smem_addr(sh.stages + s * kStageBytes);
+              ptx::mbar_arrive_expect_tx(full, kStageBytes);
+#pragma unroll
+              for (int c = 0; c < kD / kBoxCols; ++c) {
+                ptx::tma_load_2d(dst + c * kBoxBytes, &tmap, xk + c * kBoxCols, y, full);
+                ptx::tma_load_2d(dst + kHalfBytes + c * kBoxBytes, &tmap, xv + c * kBoxCols, y,
+                                 full);
+              }
+            } else {
+              atomicOr(p.status, PA_STATUS_TIMEOUT);
+              *sh.abort_flag = 1;
+            }
+          }
+          good = __shfl_sync(0xffffffffu, good, 0);
+          if (!good) {
+            ok = false;
+            break;
+          }
+          ++it;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // Let the copies already issued land before the CTA can exit.
+      for (int k = max(0, it - kStages); k < it; ++k) {
+        ptx::mbar_wait_bounded(sh.full_bar + 8 * (k % kStages), (k / kStages) & 1, kWaitLimitNs);
+      }
+    }
+    return;
+  }
+
+  // ======================= consumer warps =======================
+  const int ct = threadIdx.x;  // 0 .. kConsumers-1
+  const int gr = lane >> 2;    // head row inside the group (tensor-core layout)
+  const int tq = lane & 3;
+
+  // Empty units: output 0, LSE -inf.
+  for (int u = blockIdx.x; u < p.n_units; u += p.grid) {
+    const Unit U = p.units[u];
+    if (unit_pages(U.tok_start, U.tok_end) != 0) continue;
+    const int bt = U.bt_g / Hkv;
+    const int g = U.bt_g - bt * Hkv;
+    for (int idx = ct; idx < G * kD; idx += kConsumers) {
+      const int row = idx / kD;
+      const int d = idx - row * kD;
+      p.out[((size_t)bt * p.Hq + g * G + row) * kD + d] = 0.f;
+      if (d == 0) p.lse[(size_t)bt * p.Hq + g * G + row] = -INFINITY;
+    }
+  }
+
+  int it = 0;
+  bool ok = true;
+  for (int u = first_unit(p, cta_start); ok && u < p.n_units && p.units[u].page_first < cta_end;
+       ++u) {
+    const Unit U = p.units[u];
+    const int np = unit_pages(U.tok_start, U.tok_end);
+    if (np == 0) continue;
+    const long long pf = U.page_first;
+    const int lo = static_cast<int>(max(cta_start, pf) - pf);
+    const int hi = static_cast<int>(min(cta_end, pf + np) - pf);
+    const int bt = U.bt_g / Hkv;
+    const int g = U.bt_g - bt * Hkv;
+    const int b = bt / p.T;
+    const int first_page_tok = (U.tok_start / kPage) * kPage;
+    int poisoned = 0;
+
+    float* xo_w = sh.xo + (warp * kMaxG) * kXRow;
+    float* xml_w = sh.xml + (warp * kMaxG) * 2;
+
+    if constexpr (kTensorCores) {
+      // ---- Q fragments (A operand rows = heads; rows 8..15 stay zero) ----
+      uint32_t qa0[kD / 16], qa2[kD / 16];
+      {
+        const bool live = gr < G;
+        const __nv_bfloat16* qrow = p.q + ((size_t)b * p.Hq + g * G + (live ? gr : 0)) * kD;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          qa0[kk] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * tq)) : 0u;
+          qa2[kk] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * tq))
+                         : 0u;
+        }
+      }
+      MmaState st;
+#pragma unroll
+      for (int n = 0; n < kD / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+      st.m = -INFINITY;
+      st.l = 0.f;
+
+      const int r8 = lane & 7;
+      const int mi = lane >> 3;
+      const uint32_t k_lane = (16 * warp + (mi >> 1) * 8 + r8) * 128;
+      const int sel_k = mi & 1;
+      const uint32_t v_lane = kHalfBytes + (16 * warp + (mi & 1) * 8 + r8) * 128;
+      const int sel_v = mi >> 1;
+
+      for (int lp = lo; lp < hi; ++lp, ++it) {
+        const int s = it % kStages;
+        if (!ptx::mbar_wait_bounded(sh.full_bar + 8 * s, (it / kStages) & 1, kWaitLimitNs)) {
+          if (lane == 0) {
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+            *sh.abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        poisoned |= sh.poison[s];
+        const int page_tok = first_page_tok + lp * kPage;
+        const int vlo = max(U.tok_start, page_tok);
+        const int vhi = min(U.tok_end, page_tok + kPage);
+        const int tb = page_tok + 16 * warp;
+        const uint32_t stage = ptx::smem_addr(sh.stages + s * kStageBytes);
+        if (tb + 16 > vlo && tb < vhi) {
+          if (tb < vlo || tb + 16 > vhi) {
+            // Rows of this warp outside the tile: zero their V so that a
+            // non-finite value there cannot reach the PV product.
+            for (int r = 0; r < 16; ++r) {
+              const int tok = tb + r;
+              if (tok >= vlo && tok < vhi) continue;
+              const uint32_t a = stage + kHalfBytes + (lane >> 3) * kBoxBytes +
+                                 (16 * warp + r) * 128 + (lane & 7) * 16;
+              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u)
+                           : "memory");
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+          }
+          // ---- S = Q K^T for the warp's 16 tokens (two 8-token n-tiles) ----
+          float s0[4] = {0.f, 0.f, 0.f, 0.f};
+          float s1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const int chunk = 2 * kk + sel_k;
+            const uint32_t addr =
+                stage + (chunk >> 3) * kBoxBytes + k_lane + (((chunk & 7) ^ r8) << 4);
+            uint32_t b0, b1, b2, b3;
+            ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
+            ptx::mma_bf16_16816(s0, qa0[kk], 0u, qa2[kk], 0u, b0, b1);
+            ptx::mma_bf16_16816(s1, qa0[kk], 0u, qa2[kk], 0u, b2, b3);
+          }
+          // ---- masked online softmax (log2 domain, lazy rescale) ----
+          const bool live = gr < G;
+          const int j0 = tb + 2 * tq;
+          float x[4];
+          x[0] = (live && j0 >= vlo && j0 < vhi) ? s0[0] * p.scale_log2 : -INFINITY;
+          x[1] = (live && j0 + 1 >= vlo && j0 + 1 < vhi) ? s0[1] * p.scale_log2 : -INFINITY;
+          x[2] = (live && j0 + 8 >= vlo && j0 + 8 < vhi) ? s1[0] * p.scale_log2 : -INFINITY;
+          x[3] = (live && j0 + 9 >= vlo && j0 + 9 < vhi) ? s1[1] * p.scale_log2 : -INFINITY;
+          float bm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
+          bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
+          const bool need = bm > st.m + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            const float m_new = fmaxf(st.m, bm);
+            const float alpha = (st.m == -INFINITY) ? 0.f : exp2f(st.m - m_new);
+#pragma unroll
+            for (int n = 0; n < kD / 8; ++n) {
+              st.o[n][0] *= alpha;
+              st.o[n][1] *= alpha;
+              st.o[n][2] *= alpha;
+              st.o[n][3] *= alpha;
+            }
+            st.l *= alpha;
+            st.m = m_new;
+          }
+          const float mu = (st.m == -INFINITY) ? 0.f : st.m;
+          float pr[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) pr[k] = exp2f(x[k] - mu);
+          st.l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
+          __nv_bfloat16 ph[4], pl[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            ph[k] = __float2bfloat16_rn(pr[k]);
+            pl[k] = __float2bfloat16_rn(pr[k] - __bfloat162float(ph[k]));
+          }
+          const uint32_t pa0 = ptx::pack_bf16x2(ph[0], ph[1]);
+          const uint32_t pa1 = ptx::pack_bf16x2(pl[0], pl[1]);
+          const uint32_t pa2 = ptx::pack_bf16x2(ph[2], ph[3]);
+          const uint32_t pa3 = ptx::pack_bf16x2(pl[2], pl[3]);
+          // ---- O += P V ----
+#pragma unroll
+          for (int nd2 = 0; nd2 < kD / 16; ++nd2) {
+            const int chunk = 2 * nd2 + sel_v;
+            const uint32_t addr =
+                stage + (chunk >> 3) * kBoxBytes + v_lane + (((chunk & 7) ^ r8) << 4);
+            uint32_t b0, b1, b2, b3;
+            ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
+            ptx::mma_bf16_16816(st.o[2 * nd2], pa0, pa1, pa2, pa3, b0, b1);
+            ptx::mma_bf16_16816(st.o[2 * nd2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sh.empty_bar + 8 * s);
+      }
+      // ---- publish this warp's state for the CTA-level combine ----
+      st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
+      st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
+      if (gr < G) {
+        float* row = xo_w + gr * kXRow;
+#pragma unroll
+        for (int n = 0; n < kD / 8; ++n) {
+          *reinterpret_cast<float2*>(row + 8 * n + 2 * tq) =
+              make_float2(st.o[n][0] + st.o[n][2], st.o[n][1] + st.o[n][3]);
+        }
+        if (tq == 0) {
+          xml_w[gr * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m;
+          xml_w[gr * 2 + 1] = st.l;
+        }
+      }
+    } else {
+      // ---------------- CUDA-core variant ----------------
+      FmaState st;
+      float qf[kMaxG][8];
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        if (h < G) {
+          const uint4 raw = __ldg(reinterpret_cast<const uint4*>(
+              p.q + ((size_t)b * p.Hq + g * G + h) * kD + 8 * lane));
+          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            qf[h][2 * i] = ptx::bf16_lo_to_f32(w4[i]);
+            qf[h][2 * i + 1] = ptx::bf16_hi_to_f32(w4[i]);
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) qf[h][i] = 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) st.o[h][i] = 0.f;
+        st.m[h] = -INFINITY;
+        st.l[h] = 0.f;
+      }
+      const uint32_t lane_box = (lane >> 3) * kBoxBytes;
+      const int lane_chunk = lane & 7;
+      for (int lp = lo; lp < hi; ++lp, ++it) {
+        const int s = it % kStages;
+        if (!ptx::mbar_wait_bounded(sh.full_bar + 8 * s, (it / kStages) & 1, kWaitLimitNs)) {
+          if (lane == 0) {
+            atomicOr(p.status, PA_STATUS_TIMEOUT);
+            *sh.abort_flag = 1;
+          }
+          ok = false;
+          break;
+        }
+        poisoned |= sh.poison[s];
+        const int page_tok = first_page_tok + lp * kPage;
+        const int vlo = max(U.tok_start, page_tok);
+        const int vhi = min(U.tok_end, page_tok + kPage);
+        const int tb = page_tok + 16 * warp;
+        const uint32_t stage = ptx::smem_addr(sh.stages + s * kStageBytes);
+        const int r_lo = max(0, vlo - tb);
+        const int r_hi = min(16, vhi - tb);
+        for (int r = r_lo; r < r_hi; ++r) {
+          const int row = 16 * warp + r;
+          const uint32_t ka = stage + lane_box + row * 128 + ((lane_chunk ^ (row & 7)) << 4);
+          uint32_t k4[4], v4[4];
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(k4[0]), "=r"(k4[1]), "=r"(k4[2]), "=r"(k4[3])
+                       : "r"(ka));
+          asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                       : "=r"(v4[0]), "=r"(v4[1]), "=r"(v4[2]), "=r"(v4[3])
+                       : "r"(ka + kHalfBytes));
+          float kf[8], vf[8];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            kf[2 * i] = ptx::bf16_lo_to_f32(k4[i]);
+            kf[2 * i + 1] = ptx::bf16_hi_to_f32(k4[i]);
+            vf[2 * i] = ptx::bf16_lo_to_f32(v4[i]);
+            vf[2 * i + 1] = ptx::bf16_hi_to_f32(v4[i]);
+          }
+          float x[kMaxG];
+#pragma unroll
+          for (int h = 0; h < kMaxG; ++h) {
+            float a = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) a = fmaf(qf[h][i], kf[i], a);
+            x[h] = a;
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+#pragma unroll
+            for (int h = 0; h < kMaxG; ++h) x[h] += __shfl_xor_sync(0xffffffffu, x[h], off);
+          }
+          bool need = false;
+#pragma unroll
+          for (int h = 0; h < kMaxG; ++h) {
+            x[h] = h < G ? x[h] * p.scale_log2 : -INFINITY;
+            need |= x[h] > st.m[h] + kRescaleThreshold;
+          }
+          if (need) {  // uniform: every lane holds the same reduced scores
+#pragma unroll
+            for (int h = 0; h < kMaxG; ++h) {
+              const float m_new = fmaxf(st.m[h], x[h]);
+              const float alpha = (st.m[h] == -INFINITY) ? 0.f : exp2f(st.m[h] - m_new);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) st.o[h][i] *= alpha;
+              st.l[h] *= alpha;
+              st.m[h] = m_new;
+            }
+          }
+#pragma unroll
+          for (int h = 0; h < kMaxG; ++h) {
+            const float pr = exp2f(x[h] - (st.m[h] == -INFINITY ? 0.f : st.m[h]));
+            st.l[h] += pr;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) st.o[h][i] = fmaf(pr, vf[i], st.o[h][i]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(sh.empty_bar + 8 * s);
+      }
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        if (h < G) {
+          float* row = xo_w + h * kXRow + 8 * lane;
+          *reinterpret_cast<float4*>(row) =
+              make_float4(st.o[h][0], st.o[h][1], st.o[h][2], st.o[h][3]);
+          *reinterpret_cast<float4*>(row + 4) =
+              make_float4(st.o[h][4], st.o[h][5], st.o[h][6], st.o[h][7]);
+          if (lane == 0) {
+            xml_w[h * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m[h];
+            xml_w[h * 2 + 1] = st.l[h];
+          }
+        }
+      }
+    }
+
+    // ================= CTA-level combine of the 4 warps =================
+    ptx::named_barrier(1, kConsumers);
+    if (!ok || *sh.abort_flag) {
+      ok = false;
+      break;
+    }
+    const bool single = U.n_parts == 1;
+    int slot = 0;
+    if (!single) slot = U.part_base + (int)blockIdx.x - cta_of(pf, p.total_pages, p.grid);
+    for (int idx = ct; idx < G * kD; idx += kConsumers) {
+      const int row = idx / kD;
+      const int d = idx - row * kD;
+      float mw[kConsumerWarps];
+      float big_m = -INFINITY;
+      bool nan = false;
+#pragma unroll
+      for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+        mw[w2] = sh.xml[(w2 * kMaxG + row) * 2];
+        nan |= (mw[w2] != mw[w2]);
+        big_m = fmaxf(big_m, mw[w2]);
+      }
+      float o = 0.f, l = 0.f;
+#pragma unroll
+      for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+        const float a = (mw[w2] == -INFINITY) ? 0.f : exp2f(mw[w2] - big_m);
+        o = fmaf(a, sh.xo[(w2 * kMaxG + row) * kXRow + d], o);
+        l = fmaf(a, sh.xml[(w2 * kMaxG + row) * 2 + 1], l);
+      }
+      if (nan) big_m = __int_as_float(0x7fc00000);
+      if (single) {
+        const size_t orow = (size_t)bt * p.Hq + g * G + row;
+        p.out[orow * kD + d] = nan ? big_m : o / l;
+        if (d == 0) p.lse[orow] = nan ? big_m : (big_m + log2f(l)) * kLn2;
+      } else {
+        p.part_o[((size_t)slot * kMaxG + row) * kD + d] = o;
+        if (d == 0) {
+          p.part_ml[((size_t)slot * kMaxG + row) * 2 + 0] = big_m;
+          p.part_ml[((size_t)slot * kMaxG + row) * 2 + 1] = l;
+        }
+      }
+    }
+    if (!single) {
+      // The last CTA to finish this unit merges every partial, in CTA order.
+      __threadfence();
+      ptx::named_barrier(1, kConsumers);
+      if (ct == 0) {
+        const int prev = atomicAdd(p.counters + u, 1);
+        *sh.merge_flag = (prev == U.n_parts - 1) ? 1 : 0;
+      }
+      ptx::named_barrier(1, kConsumers);
+      if (*sh.merge_flag) {
+        __threadfence();
+        float* wts = sh.xo;                 // [part][kMaxG]
+        float* row_l = sh.xml;              // [kMaxG]
+        float* row_m = sh.xml + kMaxG;      // [kMaxG]
+        if (ct < G) {
+          const int row = ct;
+          float big_m = -INFINITY;
+          bool nan = false;
+          for (int c = 0; c < U.n_parts; ++c) {
+            const float mc = __ldcg(p.part_ml + ((size_t)(U.part_base + c) * kMaxG + row) * 2);
+            nan |= (mc != mc);
+            big_m = fmaxf(big_m, mc);
+          }
+          float l = 0.f;
+          for (int c = 0; c < U.n_parts; ++c) {
+            const float* ml = p.part_ml + ((size_t)(U.part_base + c) * kMaxG + row) * 2;
+            const float mc = __ldcg(ml);
+            const float a = (mc == -INFINITY) ? 0.f : exp2f(mc - big_m);
+            wts[c * kMaxG + row] = a;
+            l = fmaf(a, __ldcg(ml + 1), l);
+          }
+          row_l[row] = l;
+          row_m[row] = nan ? __int_as_float(0x7fc00000) : big_m;
+        }
+        ptx::named_barrier(1, kConsumers);
+        for (int idx = ct; idx < G * kD; idx += kConsumers) {
+          const int row = idx / kD;
+          const int d = idx - row * kD;
+          float o = 0.f;
+          for (int c = 0; c < U.n_parts; ++c) {
+            o = fmaf(wts[c * kMaxG + row],
+                     __ldcg(p.part_o + ((size_t)(U.part_base + c) * kMaxG + row) * kD + d), o);
+          }
+          const float big_m = row_m[row];
+          const bool nan = big_m != big_m;
+          const size_t orow = (size_t)bt * p.Hq + g * G + row;
+          p.out[orow * kD + d] = nan ? big_m : o / row_l[row];
+          if (d == 0) p.lse[orow] = nan ? big_m : (big_m + log2f(row_l[row])) * kLn2;
+        }
+        if (ct == 0) p.counters[u] = 0;
+      }
+    }
+    ptx::named_barrier(1, kConsumers);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side.
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+size_t part_slots(int B, int T, int Hkv) {
+  const long long units = (long long)B * T * Hkv;
+  return (size_t)std::min<long long>(units, kMaxUnitsLarge) + kMaxGrid;
+}
+
+size_t workspace_bytes(int B, int T, int Hkv) {
+  return kStatusBytes + kCounterBytes + part_slots(B, T, Hkv) * (kPartOBytes + kPartMLBytes);
+}
+
+template <int N, bool TC>
+cudaError_t launch(const CUtensorMap& tmap, const Params<N>& prm, int grid, cudaStream_t stream) {
+  static std::mutex mu;
+  static bool configured[64] = {false};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev >= 0 && dev < 64 && !configured[dev]) {
+      e = cudaFuncSetAttribute(paged_decode_kernel<N, TC>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+      if (e != cudaSuccess) return e;
+      configured[dev] = true;
+    }
+  }
+  paged_decode_kernel<N, TC><<<grid, kThreads, kSmemAlloc, stream>>>(tmap, prm);
+  return cudaGetLastError();
+}
+
+template <int N, bool TC>
+int launch_units(const CUtensorMap& tmap, const std::vector<Unit>& units, size_t u0, size_t n,
+                 long long total_pages, int grid, const Params<kMaxUnitsSmall>& common,
+                 cudaStream_t stream) {
+  static_assert(N >= kMaxUnitsSmall, "");
+  auto* prm = new Params<N>;
+  std::memcpy(static_cast<void*>(prm), &common, offsetof(Params<kMaxUnitsSmall>, units));
+  prm->n_units = static_cast<int>(n);
+  prm->total_pages = total_pages;
+  prm->grid = grid;
+  std::memcpy(prm->units, units.data() + u0, n * sizeof(Unit));
+  const cudaError_t e = launch<N, TC>(tmap, *prm, grid, stream);
+  delete prm;
+  if (e != cudaSuccess)
+    return fail(PA_ERR_CUDA, "paged decode launch failed: %s", cudaGetErrorString(e));
+  return PA_OK;
+}
+
+int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
+        const int32_t* page_table, int max_pages, const int32_t* tiles, int B, int T,
+        int n_q_heads, int n_kv_heads, int head_dim, float scale, float* out, float* lse,
+        void* workspace, size_t ws_bytes, cudaStream_t stream) {
+  clear_error();
+  PA_REQUIRE(B >= 0 && T >= 0, "B and T must be >= 0 (got %d, %d)", B, T);
+  if ((long long)B * T == 0) return PA_OK;
+  if (head_dim != kD)
+    return fail(PA_ERR_UNSUPPORTED, "head_dim %d not built (supported: %d)", head_dim, kD);
+  PA_REQUIRE(n_kv_heads >= 1 && n_q_heads >= n_kv_heads && n_q_heads % n_kv_heads == 0,
+             "n_q_heads (%d) must be a positive multiple of n_kv_heads (%d)", n_q_heads,
+             n_kv_heads);
+  const int G = n_q_heads / n_kv_heads;
+  if (G > kMaxG)
+    return fail(PA_ERR_UNSUPPORTED, "group size %d above the supported %d", G, kMaxG);
+  PA_REQUIRE(q && pool && page_table && tiles && out && lse && workspace,
+             "null pointer argument");
+  PA_REQUIRE(max_pages >= 1 && pool_pages >= 1, "max_pages and pool_pages must be >= 1");
+  PA_REQUIRE(reinterpret_cast<uintptr_t>(q) % 16 == 0, "q must be 16-byte aligned");
+  PA_REQUIRE(reinterpret_cast<uintptr_t>(pool) % 16 == 0, "pool must be 16-byte aligned");
+  PA_REQUIRE(reinterpret_cast<uintptr_t>(workspace) % 256 == 0,
+             "workspace must be 256-byte aligned");
+  PA_REQUIRE(pool_pages * kPage < (1ll << 31), "pool too large for 32-bit row coordinates");
+  PA_REQUIRE((long long)B * T * n_q_heads < (1ll << 31), "output too large");
+  const size_t need = workspace_bytes(B, T, n_kv_heads);
+  PA_REQUIRE(ws_bytes >= need, "workspace of %zu bytes is smaller than the %zu needed", ws_bytes,
+             need);
+  const long long max_tok = (long long)max_pages * kPage;
+  for (long long i = 0; i < (long long)B * T; ++i) {
+    const int s = tiles[2 * i], e = tiles[2 * i + 1];
+    PA_REQUIRE(s >= 0 && s <= e && e <= max_tok,
+               "tile %lld of request %lld is [%d, %d), outside [0, %lld]", i % T, i / T, s, e,
+               max_tok);
+  }
+  EncodeTiledFn enc = encode_fn();
+  if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+
+  const int row_elems = 2 * n_kv_heads * kD;
+  CUtensorMap tmap;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)row_elems, (cuuint64_t)pool_pages * kPage};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_elems * 2};
+    const cuuint32_t box[2] = {kBoxCols, kPage};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = enc(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(pool),
+                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  }
+  int sms = sm_count();
+  if (sms <= 0) return fail(PA_ERR_CUDA, "cannot query the device's SM count");
+  sms = std::min(sms, kMaxGrid);
+
+  std::vector<Unit> units;
+  units.reserve((size_t)B * T * n_kv_heads);
+  for (int bt = 0; bt < B * T; ++bt) {
+    for (int g = 0; g < n_kv_heads; ++g) {
+      Unit u{};
+      u.bt_g = bt * n_kv_heads + g;
+      u.tok_start = tiles[2 * bt];
+      u.tok_end = tiles[2 * bt + 1];
+      units.push_back(u);
+    }
+  }
+
+  Params<kMaxUnitsSmall> common{};
+  common.q = static_cast<const __nv_bfloat16*>(q);
+  common.page_table = page_table;
+  common.out = out;
+  common.lse = lse;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  common.status = reinterpret_cast<int32_t*>(ws);
+  common.counters = reinterpret_cast<int32_t*>(ws + kStatusBytes);
+  const size_t slots = part_slots(B, T, n_kv_heads);
+  common.part_o = reinterpret_cast<float*>(ws + kStatusBytes + kCounterBytes);
+  common.part_ml = reinterpret_cast<float*>(ws + kStatusBytes + kCounterBytes + slots * kPartOBytes);
+  common.pool_pages = pool_pages;
+  common.max_pages = max_pages;
+  common.T = T;
+  common.Hq = n_q_heads;
+  common.Hkv = n_kv_heads;
+  common.G = G;
+  common.scale_log2 = scale * kLog2e;
+
+  // Launches of at most kMaxUnitsLarge units each; every launch partitions its
+  // own pages and reuses the workspace after the previous one (same stream).
+  for (size_t u0 = 0; u0 < units.size(); u0 += kMaxUnitsLarge) {
+    const size_t n = std::min<size_t>(kMaxUnitsLarge, units.size() - u0);
+    long long total = 0;
+    for (size_t i = u0; i < u0 + n; ++i) {
+      units[i].page_first = static_cast<int32_t>(total);
+      total += unit_pages(units[i].tok_start, units[i].tok_end);
+      PA_REQUIRE(total < (1ll << 31), "too many pages in one launch");
+    }
+    const int grid = total > 0 ? (int)std::min<long long>(sms, total) : 1;
+    int part_cursor = 0;
+    for (size_t i = u0; i < u0 + n; ++i) {
+      const int np = unit_pages(units[i].tok_start, units[i].tok_end);
+      if (np == 0) {
+        units[i].n_parts = 0;
+        continue;
+      }
+      const int k0 = cta_of(units[i].page_first, total, grid);
+      const int k1 = cta_of(units[i].page_first + np - 1, total, grid);
+      units[i].n_parts = k1 - k0 + 1;
+      if (units[i].n_parts > 1) {
+        units[i].part_base = part_cursor;
+        part_cursor += units[i].n_parts;
+      }
+    }
+    if ((size_t)part_cursor > slots)
+      return fail(PA_ERR_INVALID, "internal: %d partial slots exceed the %zu reserved",
+                  part_cursor, slots);
+    const long long eff_total = total > 0 ? total : 1;
+    int rc;
+    if (n <= (size_t)kMaxUnitsSmall) {
+      rc = tensor_cores ? launch_units<kMaxUnitsSmall, true>(tmap, units, u0, n, eff_total, grid,
+                                                             common, stream)
+                        : launch_units<kMaxUnitsSmall, false>(tmap, units, u0, n, eff_total,
+                                                              grid, common, stream);
+    } else {
+      rc = tensor_cores ? launch_units<kMaxUnitsLarge, true>(tmap, units, u0, n, eff_total, grid,
+                                                             common, stream)
+                        : launch_units<kMaxUnitsLarge, false>(tmap, units, u0, n, eff_total,
+                                                              grid, common, stream);
+    }
+    if (rc != PA_OK) return rc;
+  }
+  return PA_OK;
+}
+
+}  // namespace decode
+}  // namespace pa
+
+extern "C" size_t paged_decode_attn_lse_workspace_bytes(int B, int T, int n_q_heads,
+                                                        int n_kv_heads, int head_dim) {
+  if (B < 0 || T < 0 || head_dim != pa::decode::kD || n_kv_heads < 1 ||
+      n_q_heads % n_kv_heads != 0 || n_q_heads / n_kv_heads > pa::decode::kMaxG)
+    return 0;
+  return pa::decode::workspace_bytes(B, T, n_kv_heads);
+}
+
+extern "C" int paged_decode_attn_lse(const void* q, const void* pool, int64_t pool_pages,
+                                     const int32_t* page_table, int max_pages,
+                                     const int32_t* tiles, int B, int T, int n_q_heads,
+                                     int n_kv_heads, int head_dim, float scale, float* out,
+                                     float* lse, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+  return pa::decode::run(true, q, pool, pool_pages, page_table, max_pages, tiles, B, T,
+                         n_q_heads, n_kv_heads, head_dim, scale, out, lse, workspace,
+                         workspace_bytes, stream);
+}
+
+extern "C" int paged_decode_attn_lse_cuda_core(const void* q, const void* pool,
+                                               int64_t pool_pages, const int32_t* page_table,
+                                               int max_pages, const int32_t* tiles, int B, int T,
+                                               int n_q_heads, int n_kv_heads, int head_dim,
+                                               float scale, float* out, float* lse,
+                                               void* workspace, size_t workspace_bytes,
+                                               cudaStream_t stream) {
+  return pa::decode::run(false, q, pool, pool_pages, page_table, max_pages, tiles, B, T,
+                         n_q_heads, n_kv_heads, head_dim, scale, out, lse, workspace,
+                         workspace_bytes, stream);
+}

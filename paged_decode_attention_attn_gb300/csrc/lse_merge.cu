@@ -1,0 +1,159 @@
+// FP32 log-sum-exp merge of per-tile partials, and the device tail-row write.
+//
+// Merge rule ("KV-cache engineering", section "Exact recent pages, compact
+// older pages"): weight each partial by exp(LSE_i - max LSE), sum the weighted
+// outputs, divide by the summed weights, and return max + log(sum) as the
+// merged LSE.  One warp per (request, head); partials are read in increasing
+// order so the result is deterministic, and the division by the summed
+// weights (not a multiply by its reciprocal) returns a single partial bit for
+// bit.  The merge reads ~H*D*4 bytes per partial once; it is tiny next to the
+// attention and is bound by L2/HBM latency, not bandwidth.
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+#include "common.h"
+
+namespace pa {
+namespace merge {
+
+constexpr int kWarpsPerBlock = 8;
+constexpr int kVecPerLane = 2;  // float4 chunks of the output row per lane per pass
+
+__global__ void __launch_bounds__(kWarpsPerBlock * 32)
+    lse_merge_kernel(const float* __restrict__ out_parts, const float* __restrict__ lse_parts,
+                     const int32_t* __restrict__ offsets, int B, int H, int D,
+                     float* __restrict__ out, float* __restrict__ lse) {
+  const int lane = threadIdx.x & 31;
+  const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (wid >= (long long)B * H) return;
+  const int b = static_cast<int>(wid / H);
+  const int h = static_cast<int>(wid - (long long)b * H);
+  const int p0 = offsets[b];
+  const int n = offsets[b + 1] - p0;
+  float* orow = out + ((size_t)b * H + h) * D;
+
+  float big_m = -INFINITY;
+  int nan = 0;
+  for (int i = lane; i < n; i += 32) {
+    const float x = lse_parts[(size_t)(p0 + i) * H + h];
+    nan |= (x != x);
+    big_m = fmaxf(big_m, x);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, off));
+    nan |= __shfl_xor_sync(0xffffffffu, nan, off);
+  }
+  const int n4 = D / 4;
+  if (nan || n <= 0 || big_m == -INFINITY) {
+    const float fill = nan ? __int_as_float(0x7fc00000) : 0.f;
+    for (int c = lane; c < n4; c += 32)
+      reinterpret_cast<float4*>(orow)[c] = make_float4(fill, fill, fill, fill);
+    if (lane == 0) lse[(size_t)b * H + h] = nan ? fill : -INFINITY;
+    return;
+  }
+  float wsum = 0.f;
+  for (int c0 = 0; c0 < n4; c0 += 32 * kVecPerLane) {
+    float4 acc[kVecPerLane];
+#pragma unroll
+    for (int v = 0; v < kVecPerLane; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ws = 0.f;
+    for (int i = 0; i < n; ++i) {
+      const float w = expf(lse_parts[(size_t)(p0 + i) * H + h] - big_m);
+      ws += w;
+      const float4* src =
+          reinterpret_cast<const float4*>(out_parts + ((size_t)(p0 + i) * H + h) * D);
+#pragma unroll
+      for (int v = 0; v < kVecPerLane; ++v) {
+        const int c = c0 + v * 32 + lane;
+        if (c < n4) {
+          const float4 x = src[c];
+          acc[v].x = fmaf(w, x.x, acc[v].x);
+          acc[v].y = fmaf(w, x.y, acc[v].y);
+          acc[v].z = fmaf(w, x.z, acc[v].z);
+          acc[v].w = fmaf(w, x.w, acc[v].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < kVecPerLane; ++v) {
+      const int c = c0 + v * 32 + lane;
+      if (c < n4)
+        reinterpret_cast<float4*>(orow)[c] =
+            make_float4(acc[v].x / ws, acc[v].y / ws, acc[v].z / ws, acc[v].w / ws);
+    }
+    wsum = ws;
+  }
+  if (lane == 0) lse[(size_t)b * H + h] = big_m + logf(wsum);
+}
+
+// One warp per row: copy rows[b] into the pool row of token positions[b].
+__global__ void append_rows_kernel(uint8_t* __restrict__ pool, long long pool_pages,
+                                   const int32_t* __restrict__ page_table, int max_pages,
+                                   const int32_t* __restrict__ positions,
+                                   const uint8_t* __restrict__ rows, int B, int row_bytes,
+                                   int32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (b >= B) return;
+  const int pos = positions[b];
+  const int lp = pos / PA_PAGE_TOKENS;
+  bool bad = pos < 0 || lp >= max_pages;
+  long long page = 0;
+  if (!bad) {
+    page = page_table[(size_t)b * max_pages + lp];
+    bad = page < 0 || page >= pool_pages;
+  }
+  if (bad) {
+    if (lane == 0 && status) atomicOr(status, PA_STATUS_BAD_ROW);
+    return;
+  }
+  uint8_t* dst = pool + ((size_t)page * PA_PAGE_TOKENS + pos % PA_PAGE_TOKENS) * row_bytes;
+  const uint8_t* src = rows + (size_t)b * row_bytes;
+  for (int c = lane; c < row_bytes / 16; c += 32)
+    reinterpret_cast<uint4*>(dst)[c] = reinterpret_cast<const uint4*>(src)[c];
+}
+
+}  // namespace merge
+}  // namespace pa
+
+extern "C" int lse_merge(const float* out_parts, const float* lse_parts,
+                         const int32_t* part_offsets, int B, int H, int D, float* out,
+                         float* lse, cudaStream_t stream) {
+  pa::clear_error();
+  PA_REQUIRE(B >= 0 && H >= 0 && D >= 0, "negative size");
+  if ((long long)B * H == 0) return PA_OK;
+  PA_REQUIRE(part_offsets && out && lse, "null pointer argument");
+  PA_REQUIRE(D % 4 == 0, "D (%d) must be a multiple of 4", D);
+  PA_REQUIRE(reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
+                 reinterpret_cast<uintptr_t>(out_parts) % 16 == 0,
+             "out and out_parts must be 16-byte aligned");
+  const long long warps = (long long)B * H;
+  const long long blocks = (warps + pa::merge::kWarpsPerBlock - 1) / pa::merge::kWarpsPerBlock;
+  PA_REQUIRE(blocks < (1ll << 31), "too many (request, head) pairs");
+  pa::merge::lse_merge_kernel<<<(unsigned)blocks, pa::merge::kWarpsPerBlock * 32, 0, stream>>>(
+      out_parts, lse_parts, part_offsets, B, H, D, out, lse);
+  PA_CHECK_CUDA(cudaGetLastError());
+  return PA_OK;
+}
+
+extern "C" int kv_append_rows(void* pool, int64_t pool_pages, const int32_t* page_table,
+                              int max_pages, const int32_t* positions, const void* rows, int B,
+                              int row_bytes, int32_t* status, cudaStream_t stream) {
+  pa::clear_error();
+  PA_REQUIRE(B >= 0, "negative B");
+  if (B == 0) return PA_OK;
+  PA_REQUIRE(pool && page_table && positions && rows, "null pointer argument");
+  PA_REQUIRE(row_bytes > 0 && row_bytes % 16 == 0, "row_bytes must be a positive multiple of 16");
+  PA_REQUIRE(reinterpret_cast<uintptr_t>(pool) % 16 == 0 &&
+                 reinterpret_cast<uintptr_t>(rows) % 16 == 0,
+             "pool and rows must be 16-byte aligned");
+  const int warps_per_block = 4;
+  const int blocks = (B + warps_per_block - 1) / warps_per_block;
+  pa::merge::append_rows_kernel<<<blocks, warps_per_block * 32, 0, stream>>>(
+      static_cast<uint8_t*>(pool), pool_pages, page_table, max_pages, positions,
+      static_cast<const uint8_t*>(rows), B, row_bytes, status);
+  PA_CHECK_CUDA(cudaGetLastError());
+  return PA_OK;
+}

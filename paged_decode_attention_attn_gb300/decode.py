@@ -1,0 +1,245 @@
+"""One decode step of paged GQA attention over every layer, on two routes.
+
+Resident route: the whole history sits in a device pool; per layer the new
+token's row is written into its page, the attention kernel returns per-tile
+(out, LSE), and the FP32 merge combines the tiles.
+
+Staged route ("Staging without a stall"; "KV-cache engineering", section
+"Staging layers under a lease"): pinned host memory owns the history; per
+layer the arena copies the layer's non-resident pages into a device slot on
+the H2D stream, the compute stream waits on the copy's event, the same three
+kernels run against the slot, attention is marked done, and only the new
+token's row is written back to its pinned host row on the D2H stream.
+
+Both routes only sequence C-ABI calls; all data movement and arithmetic run in
+libpagedattn's kernels and copies.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import binding as B
+from .workloads import DecodeWorkload, history_rows
+
+
+class _Outputs:
+    def __init__(self, w: DecodeWorkload, n_layers: int, device):
+        geo = w.geometry
+        self.tile_out = torch.empty((n_layers, w.batch, w.n_tiles, geo.n_q_heads, geo.head_dim),
+                                    dtype=torch.float32, device=device)
+        self.tile_lse = torch.empty((n_layers, w.batch, w.n_tiles, geo.n_q_heads),
+                                    dtype=torch.float32, device=device)
+        self.out = torch.empty((n_layers, w.batch, geo.n_q_heads, geo.head_dim),
+                               dtype=torch.float32, device=device)
+        self.lse = torch.empty((n_layers, w.batch, geo.n_q_heads), dtype=torch.float32,
+                               device=device)
+        self.part_offsets = torch.arange(0, (w.batch + 1) * w.n_tiles, w.n_tiles,
+                                         dtype=torch.int32, device=device)
+
+
+class ResidentDecode:
+    """Decode step over a device-resident pool [layers][pages][64][row_elems]."""
+
+    def __init__(self, w: DecodeWorkload, t: dict, cuda_core: bool = False,
+                 tiles: np.ndarray | None = None, stream=None):
+        self.w = w
+        self.t = t
+        self.cuda_core = cuda_core
+        self.tiles = np.ascontiguousarray(w.tiles if tiles is None else tiles, dtype=np.int32)
+        self.n_layers = t["pool"].shape[0]
+        dev = t["pool"].device
+        self.stream = stream
+        geo = w.geometry
+        self.o = _Outputs(w, self.n_layers, dev) if tiles is None else None
+        if self.o is None:
+            wt = DecodeWorkload(w.name, w.seed, w.n_layers, w.lengths, self.tiles, w.page_table,
+                                w.pool_pages, w.spare_pages, w.geometry)
+            self.o = _Outputs(wt, self.n_layers, dev)
+        self.workspace = B.alloc_workspace(w.batch, self.tiles.shape[1], geo.n_q_heads,
+                                           geo.n_kv_heads, geo.head_dim, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def layer(self, i: int, attention_only: bool = False):
+        t, o, geo = self.t, self.o, self.w.geometry
+        if not attention_only:
+            B.kv_append_rows(t["pool"][i], t["page_table"], t["positions"], t["new_rows"][i],
+                             status=self.status, stream=self.stream)
+        B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], self.tiles, geo.scale,
+                                o.tile_out[i], o.tile_lse[i], self.workspace,
+                                stream=self.stream, cuda_core=self.cuda_core)
+        if not attention_only:
+            B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
+                        o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
+                        o.lse[i], stream=self.stream)
+
+    def step(self):
+        for i in range(self.n_layers):
+            self.layer(i)
+
+    def kernel_status(self) -> int:
+        return int(self.workspace[:4].view(torch.int32).item()) | int(self.status.item())
+
+
+class HostHistory:
+    """Pinned host owner of every (layer, request) history segment.
+
+    Segment (l, r) holds L_r rows of row_bytes, contiguous, in logical token
+    order, as in "GPU memory management", section "A host pool that explains
+    its own size".  Row L_r - 1 is the new token's slot; the write-back fills it.
+    """
+
+    def __init__(self, w: DecodeWorkload, t: dict, layers=None):
+        geo = w.geometry
+        self.w = w
+        self.layers = list(range(t["pool"].shape[0])) if layers is None else list(layers)
+        lengths = [int(L) for L in w.lengths]
+        self.offsets = {}
+        total = 0
+        for i in range(len(self.layers)):
+            for r, L in enumerate(lengths):
+                self.offsets[(i, r)] = total
+                total += L
+        self.rows = torch.empty((total, geo.row_elems), dtype=torch.bfloat16)
+        nbytes = self.rows.numel() * 2
+        rc = torch.cuda.cudart().cudaHostRegister(self.rows.data_ptr(), nbytes, 0)
+        code = rc.value if hasattr(rc, "value") else int(rc)
+        if code != 0:
+            raise RuntimeError(f"cudaHostRegister of {nbytes} bytes failed ({rc})")
+        self._registered = True
+        for i in range(len(self.layers)):
+            for r, L in enumerate(lengths):
+                off = self.offsets[(i, r)]
+                self.rows[off:off + L].copy_(history_rows(w, t["pool"][i], r).cpu())
+        # the new token's host row is unknown until the write-back
+        for i in range(len(self.layers)):
+            for r, L in enumerate(lengths):
+                self.rows[self.offsets[(i, r)] + L - 1].zero_()
+
+    def row_address(self, i: int, r: int, row: int) -> int:
+        return self.rows.data_ptr() + (self.offsets[(i, r)] + row) * self.w.geometry.row_bytes
+
+    def row(self, i: int, r: int, row: int) -> torch.Tensor:
+        return self.rows[self.offsets[(i, r)] + row]
+
+    def close(self):
+        if getattr(self, "_registered", False):
+            torch.cuda.cudart().cudaHostUnregister(self.rows.data_ptr())
+            self._registered = False
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class StagedDecode:
+    """Decode step with host-owned history staged per layer into arena slots.
+
+    The arena is one device allocation: an optional resident window region
+    (sink + newest pages of every (layer, request), copied in once) followed
+    by ``n_slots`` staging slots each big enough for one layer's staged pages.
+    """
+
+    def __init__(self, w: DecodeWorkload, t: dict, host: HostHistory, n_slots: int = 2,
+                 cuda_core: bool = False, compute_stream=None, h2d_stream=None,
+                 d2h_stream=None):
+        geo = w.geometry
+        self.w, self.t, self.host, self.cuda_core = w, t, host, cuda_core
+        self.n_layers = t["pool"].shape[0]
+        dev = t["pool"].device
+        self.compute = compute_stream or torch.cuda.current_stream(dev)
+        self.h2d = h2d_stream or torch.cuda.Stream(dev)
+        self.d2h = d2h_stream or torch.cuda.Stream(dev)
+        self.tiles = np.ascontiguousarray(w.tiles, dtype=np.int32)
+        pt = geo.page_tokens
+        sink, recent = w.window if w.window else (0, 0)
+        self.plan = []          # per layer index: list of (request, owner, runs)
+        win_pages = 0
+        win_base = {}
+        for i in range(self.n_layers):
+            for r in range(w.batch):
+                n = w.pages_of(r)
+                if w.window and n > sink + recent:
+                    win_base[(i, r)] = win_pages
+                    win_pages += sink + recent
+        staged_max = 0
+        for i in range(self.n_layers):
+            reqs = []
+            staged = 0
+            for r in range(w.batch):
+                L, n = int(w.lengths[r]), w.pages_of(r)
+                owner = (i << 32) | r
+                if (i, r) in win_base:
+                    wb = win_base[(i, r)]
+                    mid = n - sink - recent
+                    runs = [dict(logical_page=0, n_pages=sink, resident_page=wb),
+                            dict(logical_page=sink, n_pages=mid, n_rows=mid * pt,
+                                 host_rows=host.row_address(i, r, sink * pt)),
+                            dict(logical_page=n - recent, n_pages=recent,
+                                 resident_page=wb + sink)]
+                    staged += mid
+                else:
+                    runs = [dict(logical_page=0, n_pages=n, n_rows=L - 1,
+                                 host_rows=host.row_address(i, r, 0))]
+                    staged += n
+                reqs.append((r, owner, runs))
+            staged_max = max(staged_max, staged)
+            self.plan.append(reqs)
+        self.win_pages = win_pages
+        self.slot_pages = max(1, staged_max)
+        arena_pages = win_pages + n_slots * self.slot_pages
+        self.arena = torch.empty((arena_pages, pt, geo.row_elems), dtype=torch.bfloat16,
+                                 device=dev)
+        self.arena.fill_(float("nan"))          # canary: unwritten rows read as NaN
+        for (i, r), wb in win_base.items():     # resident window copied in once
+            n = w.pages_of(r)
+            idx = list(range(sink)) + list(range(n - recent, n))
+            phys = torch.as_tensor(w.page_table[r, idx], dtype=torch.long, device=dev)
+            self.arena[wb:wb + sink + recent] = t["pool"][i].index_select(0, phys)
+        self.page_tables = torch.zeros((n_slots, w.batch, w.max_pages), dtype=torch.int32,
+                                       device=dev)
+        torch.cuda.synchronize(dev)
+        self.handle = B.Arena(self.arena.data_ptr(), self.arena.numel() * 2, geo.row_bytes,
+                              n_slots, win_pages, self.slot_pages, self.page_tables.data_ptr(),
+                              w.batch, w.max_pages, compute_stream=self.compute,
+                              h2d_stream=self.h2d, d2h_stream=self.d2h)
+        self.o = _Outputs(w, self.n_layers, dev)
+        self.workspace = B.alloc_workspace(w.batch, w.n_tiles, geo.n_q_heads, geo.n_kv_heads,
+                                           geo.head_dim, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.tails = []
+        for i in range(self.n_layers):
+            self.tails.append([(r, int(w.lengths[r]) - 1,
+                                host.row_address(i, r, int(w.lengths[r]) - 1), (i << 32) | r)
+                               for r in range(w.batch)])
+
+    def layer(self, i: int):
+        t, o, geo = self.t, self.o, self.w.geometry
+        slot, _ = self.handle.stage_layer(i, self.plan[i])
+        table = self.page_tables[slot]
+        B.kv_append_rows(self.arena, table, t["positions"], t["new_rows"][i], status=self.status,
+                         stream=self.compute)
+        B.paged_decode_attn_lse(t["q"][i], self.arena, table, self.tiles, geo.scale,
+                                o.tile_out[i], o.tile_lse[i], self.workspace,
+                                stream=self.compute, cuda_core=self.cuda_core)
+        B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
+                    o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i], o.lse[i],
+                    stream=self.compute)
+        self.handle.mark_attention_done(i)
+        self.handle.writeback_tail(i, self.tails[i])
+
+    def step(self):
+        for i in range(self.n_layers):
+            self.layer(i)
+
+    def drain(self):
+        self.handle.drain()
+
+    def kernel_status(self) -> int:
+        return int(self.workspace[:4].view(torch.int32).item()) | int(self.status.item())
+
+    def close(self):
+        self.handle.close()

@@ -1,0 +1,92 @@
+"""C-ABI checks that need no GPU: every declared symbol is exported, and the
+host-side argument checks refuse bad calls before anything reaches CUDA."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedattn.h")
+
+
+@pytest.fixture(scope="module")
+def B():
+    from paged_decode_attention_attn_gb300 import build
+    build.build()
+    from paged_decode_attention_attn_gb300 import binding
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("kv_arena_create", "kv_stage_layer", "paged_decode_attn_lse", "lse_merge",
+                     "kv_writeback_tail", "kv_arena_destroy", "kv_arena_drain",
+                     "kv_mark_attention_done", "kv_last_error"):
+        assert required in names
+
+
+def test_every_declared_symbol_is_exported(B):
+    names = declared_functions()
+    assert names, "no declarations parsed"
+    for name in names:
+        assert hasattr(B.lib, name), f"{name} declared in pagedattn.h but not exported"
+    assert sorted(names) == sorted(B.EXPORTED)
+
+
+def test_version_string(B):
+    assert b"sm_103a" in B.lib.pa_version()
+
+
+def test_workspace_query(B):
+    n = B.workspace_bytes(4, 1, 24, 4, 256)
+    assert n > 0 and n % 256 == 0
+    assert B.workspace_bytes(4, 1, 24, 4, 128) == 0        # head_dim not built
+    assert B.workspace_bytes(4, 1, 36, 4, 256) == 0        # group 9 > 8
+    assert B.workspace_bytes(4, 1, 25, 4, 256) == 0        # not a multiple
+
+
+def _call_decode(B, tiles, head_dim=256, nq=24, nkv=4, ws_bytes=1 << 30, ws_ptr=1 << 20,
+                 pool_pages=16, max_pages=8):
+    arr = np.ascontiguousarray(np.asarray(tiles, dtype=np.int32))
+    Bn, T = arr.shape[0], arr.shape[1]
+    fake = 1 << 20  # never dereferenced: the checks below fail before any CUDA call
+    return B.lib.paged_decode_attn_lse(fake, fake, pool_pages, fake, max_pages, arr.ctypes.data,
+                                       Bn, T, nq, nkv, head_dim, 0.0625, fake, fake, ws_ptr,
+                                       ws_bytes, None)
+
+
+def test_decode_argument_checks(B):
+    ok_tiles = [[[0, 64]]]
+    assert _call_decode(B, ok_tiles, head_dim=128) == B.PA_ERR_UNSUPPORTED
+    assert _call_decode(B, ok_tiles, nq=25) == B.PA_ERR_INVALID
+    assert _call_decode(B, ok_tiles, nq=72) == B.PA_ERR_UNSUPPORTED
+    assert _call_decode(B, [[[0, 8 * 64 + 1]]]) == B.PA_ERR_INVALID     # past the table
+    assert _call_decode(B, [[[10, 5]]]) == B.PA_ERR_INVALID             # start > end
+    assert _call_decode(B, [[[-1, 5]]]) == B.PA_ERR_INVALID
+    assert _call_decode(B, ok_tiles, ws_bytes=1024) == B.PA_ERR_INVALID  # workspace too small
+    assert _call_decode(B, ok_tiles, ws_ptr=(1 << 20) + 16) == B.PA_ERR_INVALID  # misaligned
+    assert "workspace" in B.last_error()
+    # zero requests is a no-op
+    arr = np.zeros((0, 1, 2), dtype=np.int32)
+    assert B.lib.paged_decode_attn_lse(0, 0, 0, 0, 0, arr.ctypes.data, 0, 1, 24, 4, 256, 1.0, 0,
+                                       0, 0, 0, None) == B.PA_OK
+
+
+def test_merge_and_append_argument_checks(B):
+    fake = 1 << 20
+    assert B.lib.lse_merge(fake, fake, fake, 2, 24, 254, fake, fake, None) == B.PA_ERR_INVALID
+    assert B.lib.lse_merge(fake, fake, fake, 0, 24, 256, fake, fake, None) == B.PA_OK
+    assert B.lib.kv_append_rows(fake, 4, fake, 4, fake, fake, 1, 4008, None, None) == \
+        B.PA_ERR_INVALID
+    assert B.lib.kv_append_rows(fake, 4, fake, 4, fake, fake + 8, 1, 4096, None, None) == \
+        B.PA_ERR_INVALID

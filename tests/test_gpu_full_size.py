@@ -1,0 +1,107 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration the
+bench times (one attention launch per layer, persistent grid of one CTA per
+SM), and bit-identity of the host-staged route against the resident route.
+
+The oracle checks sampled (layer, request) pairs one by one; properties that
+hold at any size (finite outputs, status word clear, tiled+merged equal to the
+single-tile result within 1e-5, staged equal to resident bit for bit, tail
+write-back equal to the new row bit for bit) are checked on every output.
+"""
+
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from paged_decode_attention_attn_gb300 import workloads as wl
+from parity_utils import TOL_SPLIT, assert_close_to_oracle, max_abs, oracle_request
+
+pytestmark = pytest.mark.gpu
+
+FULL = {
+    "4x31744": (wl.four_requests_31744, [(0, 1), (15, 3)]),
+    "1x262144": (wl.one_request_262144, [(7, 0)]),
+    "ragged-window": (wl.ragged_window, [(3, "longest"), (12, "shortest")]),
+}
+
+
+@pytest.fixture(scope="module")
+def D():
+    from paged_decode_attention_attn_gb300 import build
+    build.build()
+    from paged_decode_attention_attn_gb300 import decode
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return decode
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_resident_matches_oracle(D, name):
+    make, samples = FULL[name]
+    w = make()
+    t = wl.materialize(w, "cuda")
+    dec = D.ResidentDecode(w, t)
+    dec.step()
+    torch.cuda.synchronize()
+    assert dec.kernel_status() == 0
+    o = dec.o
+    real = torch.as_tensor(w.tiles[:, :, 1] > w.tiles[:, :, 0], device="cuda")
+    assert torch.isfinite(o.out).all() and torch.isfinite(o.lse).all()
+    assert torch.isfinite(o.tile_out[:, real]).all()
+    for i, r in samples:
+        if r == "longest":
+            r = int(np.argmax(w.lengths))
+        elif r == "shortest":
+            r = int(np.argmin(w.lengths))
+        ref = oracle_request(w, t, i, r, gather_on_device=True)
+        assert_close_to_oracle(o.tile_out[i, r], o.tile_lse[i, r], o.out[i, r], o.lse[i, r], ref,
+                               w.tiles[r], f"{name} layer {i} request {r}")
+    if w.n_tiles > 1:
+        single = np.zeros((w.batch, 1, 2), dtype=np.int32)
+        single[:, 0, 1] = w.lengths
+        one = D.ResidentDecode(w, t, tiles=single)
+        for i in range(w.n_layers):
+            one.layer(i, attention_only=True)
+        torch.cuda.synchronize()
+        assert max_abs(one.o.tile_out[:, :, 0].cpu(), o.out.cpu()) <= TOL_SPLIT
+        assert max_abs(one.o.tile_lse[:, :, 0].cpu(), o.lse.cpu()) <= TOL_SPLIT
+        del one
+    del dec, t, o
+    _free()
+
+
+@pytest.mark.parametrize("name,n_slots", [("4x31744", 2), ("4x31744", 1), ("1x262144", 2),
+                                          ("ragged-window", 2)])
+def test_staged_route_is_bit_identical_to_resident(D, name, n_slots):
+    make, _ = FULL[name]
+    w = make(n_layers=3)
+    t = wl.materialize(w, "cuda")
+    host = D.HostHistory(w, t)
+    staged = D.StagedDecode(w, t, host, n_slots=n_slots)
+    res = D.ResidentDecode(w, t)
+    res.step()
+    torch.cuda.synchronize()
+    staged.step()
+    staged.drain()
+    torch.cuda.synchronize()
+    assert res.kernel_status() == 0 and staged.kernel_status() == 0
+    assert torch.equal(staged.o.tile_out, res.o.tile_out)
+    assert torch.equal(staged.o.tile_lse, res.o.tile_lse)
+    assert torch.equal(staged.o.out, res.o.out)
+    assert torch.equal(staged.o.lse, res.o.lse)
+    for i in range(w.n_layers):
+        for r in range(w.batch):
+            row = host.row(i, r, int(w.lengths[r]) - 1)
+            assert torch.equal(row.view(torch.int16), t["new_rows"][i, r].cpu().view(torch.int16))
+    st = staged.handle.stats()
+    assert st.stage_generation == w.n_layers and st.quarantined == 0
+    assert st.written_back_bytes == w.n_layers * w.batch * w.geometry.row_bytes
+    staged.close()
+    host.close()
+    del staged, res, host, t
+    _free()

@@ -1,0 +1,234 @@
+"""GPU parity of the CUDA path against the fp64 oracle on small and edge cases.
+
+Every call goes through the C-ABI library (ctypes binding).  Tolerances:
+max-abs 2e-3 on outputs and 1e-4 on LSE against the oracle; 1e-5 between a
+tiled+merged result and the single-tile result; bit equality where only the
+physical placement of pages differs.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_decode_attention_attn_gb300 import workloads as wl
+from parity_utils import (TOL_LSE, TOL_OUT, TOL_SPLIT, assert_close_to_oracle, bits, max_abs,
+                          oracle_request)
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = [False, True]   # cuda_core flag: tensor-core kernel, CUDA-core kernel
+VARIANT_IDS = ["tensor_core", "cuda_core"]
+
+
+@pytest.fixture(scope="module")
+def B():
+    from paged_decode_attention_attn_gb300 import build
+    build.build()
+    from paged_decode_attention_attn_gb300 import binding
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return binding
+
+
+@pytest.fixture(scope="module")
+def D(B):
+    from paged_decode_attention_attn_gb300 import decode
+    return decode
+
+
+def run_resident(D, w, t, cuda_core, tiles=None):
+    dec = D.ResidentDecode(w, t, cuda_core=cuda_core, tiles=tiles)
+    dec.step()
+    torch.cuda.synchronize()
+    assert dec.kernel_status() == 0
+    return dec
+
+
+@pytest.mark.parametrize("cuda_core", VARIANTS, ids=VARIANT_IDS)
+def test_tiny_decode_matches_oracle(B, D, cuda_core):
+    w = wl.tiny_decode(seed=0)
+    t = wl.materialize(w, "cuda")
+    dec = run_resident(D, w, t, cuda_core)
+    ref = oracle_request(w, t, 0, 0)
+    o = dec.o
+    assert torch.isfinite(o.tile_out).all() and torch.isfinite(o.out).all()
+    assert_close_to_oracle(o.tile_out[0, 0], o.tile_lse[0, 0], o.out[0, 0], o.lse[0, 0], ref,
+                           w.tiles[0], "tiny")
+    # one tile over the whole history vs four tiles merged
+    single = run_resident(D, w, t, cuda_core, tiles=np.array([[[0, 2048]]], dtype=np.int32))
+    assert max_abs(single.o.tile_out[0, 0, 0].cpu(), o.out[0, 0].cpu()) <= TOL_SPLIT
+    assert max_abs(single.o.tile_lse[0, 0, 0].cpu(), o.lse[0, 0].cpu()) <= TOL_SPLIT
+    assert max_abs(single.o.tile_out[0, 0, 0].double().cpu(), ref["unsplit_out"]) <= TOL_OUT
+    assert max_abs(single.o.tile_lse[0, 0, 0].double().cpu(), ref["unsplit_lse"]) <= TOL_LSE
+
+
+def edge_workload():
+    lengths = [1, 63, 64, 65, 150, 1000, 4097]
+    tiles = [
+        [(0, 1), (0, 0)],
+        [(0, 63), (5, 6), (62, 63)],
+        [(0, 64), (0, 32), (32, 64)],
+        [(0, 65), (64, 65), (0, 64)],
+        [(37, 101), (0, 150), (100, 150), (149, 150)],
+        [(0, 1000), (0, 333), (333, 1000), (1, 999), (500, 500)],
+        [(0, 4097), (4096, 4097), (63, 2049), (0, 4096)],
+    ]
+    return wl.custom(lengths, tiles, seed=21, n_spare=5, max_pages=70)
+
+
+@pytest.mark.parametrize("cuda_core", VARIANTS, ids=VARIANT_IDS)
+def test_edge_cases_match_oracle(B, D, cuda_core):
+    w = edge_workload()
+    t = wl.materialize(w, "cuda")
+    dec = run_resident(D, w, t, cuda_core)
+    o = dec.o
+    for r in range(w.batch):
+        ref = oracle_request(w, t, 0, r)
+        assert_close_to_oracle(o.tile_out[0, r], o.tile_lse[0, r], o.out[0, r], o.lse[0, r],
+                               ref, w.tiles[r], f"request {r}")
+
+
+@pytest.mark.parametrize("cuda_core", VARIANTS, ids=VARIANT_IDS)
+def test_physical_placement_does_not_change_bits(B, D, cuda_core):
+    w = wl.custom([3000, 777, 64], [[(0, 3000), (100, 2000)], [(0, 777)], [(0, 64)]], seed=5,
+                  n_spare=7)
+    t = wl.materialize(w, "cuda")
+    a = run_resident(D, w, t, cuda_core)
+    # move every page to a new physical slot, rebuild the page table accordingly
+    perm = np.random.default_rng(9).permutation(w.pool_pages)
+    t2 = dict(t)
+    pool2 = torch.empty_like(t["pool"])
+    pool2[:, torch.as_tensor(perm, device="cuda")] = t["pool"]
+    t2["pool"] = pool2
+    table2 = w.page_table.copy()
+    n_used = [w.pages_of(r) for r in range(w.batch)]
+    for r in range(w.batch):
+        table2[r, :n_used[r]] = perm[w.page_table[r, :n_used[r]]]
+    w2 = wl.DecodeWorkload(w.name, w.seed, w.n_layers, w.lengths, w.tiles, table2, w.pool_pages,
+                           perm[w.spare_pages], w.geometry)
+    t2["page_table"] = torch.as_tensor(table2, device="cuda")
+    b = run_resident(D, w2, t2, cuda_core)
+    assert torch.equal(a.o.tile_out, b.o.tile_out)
+    assert torch.equal(a.o.tile_lse, b.o.tile_lse)
+    assert torch.equal(a.o.out, b.o.out) and torch.equal(a.o.lse, b.o.lse)
+
+
+def test_variants_agree(B, D):
+    w = edge_workload()
+    t = wl.materialize(w, "cuda")
+    a = run_resident(D, w, t, False)
+    b = run_resident(D, w, t, True)
+    assert max_abs(a.o.out.cpu(), b.o.out.cpu()) <= 2 * TOL_SPLIT
+    assert max_abs(a.o.lse.cpu(), b.o.lse.cpu()) <= 2 * TOL_SPLIT
+
+
+@pytest.mark.parametrize("cuda_core", VARIANTS, ids=VARIANT_IDS)
+def test_bad_page_id_is_reported_not_read(B, D, cuda_core):
+    w = wl.custom([640, 640], [[(0, 320), (320, 640)], [(0, 640), (0, 0)]], seed=3, n_spare=2)
+    t = wl.materialize(w, "cuda")
+    t["page_table"][0, 7] = w.pool_pages + 1000     # page 7 = tokens [448, 512)
+    dec = D.ResidentDecode(w, t, cuda_core=cuda_core)
+    dec.layer(0)
+    torch.cuda.synchronize()
+    assert dec.kernel_status() & B.PA_STATUS_BAD_PAGE
+    o = dec.o
+    assert torch.isnan(o.tile_out[0, 0, 1]).all() and torch.isnan(o.tile_lse[0, 0, 1]).all()
+    assert torch.isfinite(o.tile_out[0, 0, 0]).all()        # tile 0 never touches page 7
+    assert torch.isfinite(o.tile_out[0, 1]).all()
+    ref = oracle_request(w, t, 0, 1)
+    assert_close_to_oracle(o.tile_out[0, 1], o.tile_lse[0, 1], None, None, ref, w.tiles[1])
+
+
+def test_append_rows_writes_exact_bytes(B):
+    w = wl.custom([100, 64, 3], [[(0, 100)], [(0, 64)], [(0, 3)]], seed=4, n_spare=1)
+    t = wl.materialize(w, "cuda")
+    pool = t["pool"][0]
+    before = pool.clone()
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.kv_append_rows(pool, t["page_table"], t["positions"], t["new_rows"][0], status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    changed = (pool.view(torch.int16) != before.view(torch.int16)).any(dim=-1)
+    for r in range(w.batch):
+        pos = int(w.lengths[r]) - 1
+        page, row = int(w.page_table[r, pos // 64]), pos % 64
+        assert torch.equal(pool[page, row].view(torch.int16), t["new_rows"][0, r].view(torch.int16))
+        changed[page, row] = False
+    assert not changed.any()                        # nothing else was written
+    bad = torch.tensor([5000, 1, 2], dtype=torch.int32, device="cuda")
+    before = pool.clone()
+    B.kv_append_rows(pool, t["page_table"], bad, t["new_rows"][0], status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & B.PA_STATUS_BAD_ROW
+    # request 0 (position past its page table) is skipped; 1 and 2 land at rows 1 and 2
+    changed = (pool.view(torch.int16) != before.view(torch.int16)).any(dim=-1)
+    for r, pos in ((1, 1), (2, 2)):
+        page = int(w.page_table[r, 0])
+        assert torch.equal(pool[page, pos].view(torch.int16), t["new_rows"][0, r].view(torch.int16))
+        changed[page, pos] = False
+    assert not changed.any()
+
+
+def merge_inputs_from_oracle(case, requests):
+    outs, lses, offsets, targets = [], [], [0], []
+    for r in requests:
+        o, l, t_out, t_lse = oracle.merge_stress_partials(case.tile_logits[r], case.tile_values[r],
+                                                          case.tile_bias[r])
+        outs.append(o)
+        lses.append(l)
+        offsets.append(offsets[-1] + o.shape[0])
+        targets.append((t_out, t_lse))
+    return (np.concatenate(outs), np.concatenate(lses), np.array(offsets, dtype=np.int32),
+            targets)
+
+
+def test_lse_merge_stress_matches_unsplit_softmax(B):
+    case = wl.merge_stress(seed=5)
+    outs, lses, offsets, targets = merge_inputs_from_oracle(case, range(len(case.tile_logits)))
+    assert np.ptp(lses) > 100                         # the +-80 spread is there
+    dev = "cuda"
+    op = torch.as_tensor(outs, dtype=torch.float32, device=dev)
+    lp = torch.as_tensor(lses, dtype=torch.float32, device=dev)
+    off = torch.as_tensor(offsets, device=dev)
+    nb = len(targets)
+    out = torch.empty((nb, case.n_heads, case.head_dim), dtype=torch.float32, device=dev)
+    lse = torch.empty((nb, case.n_heads), dtype=torch.float32, device=dev)
+    B.lse_merge(op, lp, off, out, lse)
+    torch.cuda.synchronize()
+    worst_o = worst_l = 0.0
+    for r, (t_out, t_lse) in enumerate(targets):
+        worst_o = max(worst_o, max_abs(out[r].double().cpu(), t_out))
+        worst_l = max(worst_l, max_abs(lse[r].double().cpu(), t_lse))
+    assert worst_o <= TOL_OUT and worst_l <= TOL_LSE, (worst_o, worst_l)
+    # the same partials through the oracle's own merge (fp32 inputs) agree too
+    o32 = op.double().cpu().numpy()
+    l32 = lp.double().cpu().numpy()
+    for r in (0, nb // 2, nb - 1):
+        mo, ml = oracle.lse_merge(o32[offsets[r]:offsets[r + 1]], l32[offsets[r]:offsets[r + 1]])
+        assert max_abs(out[r].double().cpu(), mo) <= 1e-5
+        assert max_abs(lse[r].double().cpu(), ml) <= 1e-4
+
+
+def test_lse_merge_identity_and_edges(B):
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(1)
+    H, D = 24, 256
+    parts = torch.randn((4, H, D), generator=g, device=dev)
+    lses = torch.randn((4, H), generator=g, device=dev) * 40
+    lses[2] = -float("inf")                    # request 2: all -inf
+    lses[3, 5] = float("nan")                  # request 3: one NaN head
+    # requests: 0 -> [0,1) single; 1 -> [1,1) none; 2 -> [2,3) all -inf; 3 -> [3,4) nan
+    off = torch.tensor([0, 1, 1, 2, 3, 4], dtype=torch.int32, device=dev)
+    nb = 5
+    out = torch.full((nb, H, D), 7.0, device=dev)
+    lse = torch.full((nb, H), 7.0, device=dev)
+    parts5 = torch.cat([parts[0:1], parts[2:3], parts[1:2], parts[3:4]])
+    lses5 = torch.cat([lses[0:1], lses[2:3], lses[1:2], lses[3:4]])
+    B.lse_merge(parts5, lses5, off, out, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(out[0], parts5[0]) and torch.equal(lse[0], lses5[0])   # bitwise identity
+    assert torch.all(out[1] == 0) and torch.all(lse[1] == -float("inf"))      # no partials
+    assert torch.all(out[2] == 0) and torch.all(lse[2] == -float("inf"))      # all -inf
+    assert torch.equal(out[3], parts5[2]) and torch.equal(lse[3], lses5[2])
+    assert torch.isnan(lse[4, 5]) and torch.isnan(out[4, 5]).all()
+    assert torch.isfinite(out[4, :5]).all()
