@@ -46,8 +46,11 @@ KERNEL_SOURCE = os.path.join(ROOT, "paged_decode_attention_attn_gb300", "csrc", 
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--layers", type=int, default=16,
+                    help="layers of the workload (16 is the benchmarked workload; fewer "
+                         "layers only make small profiling cases)")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cuda-core", action="store_true",
                     help="time the CUDA-core attention kernel instead of the tensor-core one")
@@ -94,52 +97,52 @@ def max_over_ranks(x, world):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
+    """nvidia-smi in loop mode (every 100 ms) for the duration of the region."""
+
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
         self.index = index
-        self.samples = []
-        self._stop = threading.Event()
-        self._thread = None
+        self.proc = None
 
     def start(self):
-        self._thread = threading.Thread(target=self._run, daemon=True)
-        self._thread.start()
-
-    def _run(self):
-        while not self._stop.is_set():
-            try:
-                out = subprocess.run(
-                    ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                     "--format=csv,noheader,nounits"], capture_output=True, text=True,
-                    timeout=5).stdout.strip()
-                if out:
-                    self.samples.append([x.strip() for x in out.split(",")])
-            except Exception:
-                pass
-            self._stop.wait(0.2)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
 
     def stop(self):
-        self._stop.set()
-        if self._thread:
-            self._thread.join(timeout=10)
-        sm = []
+        rows = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=10)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            rows = [[x.strip() for x in line.split(",")] for line in out.splitlines() if line]
+        sm, power = [], []
         mx = 0.0
         reasons = set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for s in self.samples:
+        for s in rows:
             try:
                 sm.append(float(s[0]))
                 mx = max(mx, float(s[1]))
+                power.append(float(s[2]))
             except (ValueError, IndexError):
                 continue
             for name, val in zip(names, s[4:8]):
                 if val.strip().lower() == "active":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
 
 
 # ---------------------------------------------------------------------------
@@ -275,7 +278,7 @@ def run_ours(args):
     from paged_decode_attention_attn_gb300 import decode as D
     from paged_decode_attention_attn_gb300 import workloads as wl
 
-    w = wl.four_requests_31744()
+    w = wl.four_requests_31744(n_layers=args.layers)
     t = wl.materialize(w, dev)
     geo = w.geometry
     kv_bytes = w.kv_bytes_per_step()
@@ -283,45 +286,60 @@ def run_ours(args):
     stream = torch.cuda.current_stream(dev)
     res = D.ResidentDecode(w, t, cuda_core=args.cuda_core, stream=stream)
 
-    # ---- resident route: value + roofline ----
+    # ---- resident route: value (CUDA-graph replay of the whole step) ----
     n_ev = args.steps * w.n_layers
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_ev)]
 
-    def resident_step(step_idx):
+    def resident_step(step_idx, s):
         o = res.o
         for i in range(w.n_layers):
             B.kv_append_rows(t["pool"][i], t["page_table"], t["positions"], t["new_rows"][i],
-                             status=res.status, stream=stream)
+                             status=res.status, stream=s)
             if step_idx is not None:
-                ev[step_idx * w.n_layers + i][0].record(stream)
+                ev[step_idx * w.n_layers + i][0].record(s)
             B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], res.tiles,
                                     geo.scale, o.tile_out[i], o.tile_lse[i], res.workspace,
-                                    stream=stream, cuda_core=args.cuda_core)
+                                    stream=s, cuda_core=args.cuda_core)
             if step_idx is not None:
-                ev[step_idx * w.n_layers + i][1].record(stream)
+                ev[step_idx * w.n_layers + i][1].record(s)
             B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
                         o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
-                        o.lse[i], stream=stream)
+                        o.lse[i], stream=s)
 
     for _ in range(max(3, args.warmup)):
-        resident_step(None)
+        resident_step(None, stream)
     torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        resident_step(None, cap)
+    torch.cuda.synchronize(dev)
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize(dev)
+
     clocks = ClockSampler(local)
     clocks.start()
-    time.sleep(0.5)
     barrier(world)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
-    for k in range(args.steps):
-        resident_step(k)
+    host_t0 = time.perf_counter()
+    for _ in range(args.steps):
+        graph.replay()
+    host_issue_s = time.perf_counter() - host_t0
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
-    clk = clocks.stop()
     elapsed_ms = start.elapsed_time(end)
-    # attention-kernel launch times, recorded around each launch in the timed region
+    # ---- roofline of the attention kernel: events around every launch of an
+    # eager run of the same steps (a second timed region, same clocks record) ----
+    for k in range(args.steps):
+        resident_step(k, stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
     kernel_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     status = res.kernel_status()
     if status != 0:
@@ -367,6 +385,8 @@ def run_ours(args):
                          "bytes_per_launch": kv_bytes_layer,
                          "mean_launch_ms": round(kern_ms, 5)},
             "clocks": clk,
+            "host_issue_ms_per_step": round(1e3 * host_issue_s / args.steps, 4),
+            "step_launch": "CUDA graph of the 48 launches of one step, replayed per step",
         }
         if e2e is not None:
             line["e2e"] = e2e
@@ -413,6 +433,20 @@ def run_e2e(args, w, t, dev, D, B):
         raise RuntimeError("staged route kernel status non-zero")
     stats = st.handle.stats()
     staged_per_step = stats.staged_bytes // stats.stage_generation * w.n_layers
+    # host-link probe: the first layer's host history copied H2D on one stream
+    seg = host.rows[: sum(int(L) for L in w.lengths)]
+    dst = torch.empty(seg.shape, dtype=seg.dtype, device=dev)
+    ps = torch.cuda.Stream(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(ps):
+        dst.copy_(seg, non_blocking=True)
+        e0.record(ps)
+        for _ in range(3):
+            dst.copy_(seg, non_blocking=True)
+        e1.record(ps)
+    torch.cuda.synchronize(dev)
+    probe_gbs = 3 * seg.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
+    del dst
     h2d = q_host.numel() * 2 + rows_host.numel() * 2 + staged_per_step
     d2h = out_host.numel() * 4 + lse_host.numel() * 4 + w.n_layers * w.batch * geo.row_bytes
     kv = w.kv_bytes_per_step()
@@ -420,7 +454,8 @@ def run_e2e(args, w, t, dev, D, B):
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
            "route": "host-staged, 2 arena slots, tail write-back",
            "ms_per_step": round(1e3 * secs / steps, 3),
-           "h2d_GBps": round(staged_per_step * steps / secs / 1e9, 2), "steps": steps}
+           "h2d_GBps": round(staged_per_step * steps / secs / 1e9, 2),
+           "link_probe_h2d_GBps": round(probe_gbs, 2), "steps": steps}
     st.close()
     host.close()
     return res

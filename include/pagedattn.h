@@ -109,7 +109,8 @@ size_t paged_decode_attn_lse_workspace_bytes(int B, int T, int n_q_heads,
  *   tiles      HOST int32 [B][T][2]; 0 <= start <= end <= max_pages*64 is
  *              checked (PA_ERR_INVALID).  Tiles may overlap and need not be
  *              page aligned; rows outside a tile are masked, whatever they hold.
- *   out, lse   device fp32 [B][T][n_q_heads][head_dim] and [B][T][n_q_heads].
+ *   out, lse   device fp32 [B][T][n_q_heads][head_dim] (16-byte aligned) and
+ *              [B][T][n_q_heads].
  *   workspace  device buffer of at least the bytes the query above returns,
  *              256-byte aligned, ZERO-FILLED before its first use; every call
  *              leaves it ready for the next (counters return to zero).  Byte 0

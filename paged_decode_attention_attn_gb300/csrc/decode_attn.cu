@@ -19,14 +19,19 @@
 //    slice of one kv head (64 rows x 512 B each, row stride 4 KiB) as eight
 //    64x64 boxes with the 128-byte swizzle, into a 3-stage mbarrier ring
 //    (64 KiB per stage).
-//  * Four consumer warps each take 16 tokens of every page.  All G <= 8 query
-//    heads of the GQA group share the page, so the grouped scores are a
-//    16 x 8 x 256 product per warp (tensor-core mma.sync m16n8k16, heads as
-//    rows, bf16 in, fp32 accumulate).  Online softmax runs in the log2 domain
-//    with a lazy rescale (the running reference only moves when the max grows
-//    by more than 2^8).  P enters the PV product as a hi + lo pair of bf16
-//    values packed into the otherwise idle rows 8..15 of the A tile, which
-//    keeps ~16 significant bits of every probability at no extra MMA cost.
+//  * Eight consumer warps: each 16-token group of a page is taken by two
+//    warps that compute the same grouped scores and split the 256 output
+//    dims, so every SM sub-partition interleaves two consumer warps.  All
+//    G <= 8 query heads of the GQA group share the page, so the grouped
+//    scores are a 16 x 8 x 256 product per warp (tensor-core mma.sync
+//    m16n8k16, heads as rows, bf16 in, fp32 accumulate).  Online softmax runs
+//    in the log2 domain against a reference kept on multiples of 8, so it
+//    moves (an exact power-of-two rescale) only when the max crosses the next
+//    multiple.  P enters the PV product as a hi + lo pair of bf16 values
+//    packed into the otherwise idle rows 8..15 of the A tile (~16 significant
+//    bits of every probability at no extra MMA cost); each page's PV product
+//    starts from zero and is added to the running output with fp32
+//    round-to-nearest adds.
 //  * A CUDA-core variant (FP32 FMAs, one lane per 8 dims) runs the same
 //    pipeline; it exists to measure the tensor-core choice against.
 #include <cuda.h>
@@ -49,16 +54,14 @@ constexpr int kPage = PA_PAGE_TOKENS;                    // tokens per page
 constexpr int kD = 256;                                  // head_dim
 constexpr int kMaxG = 8;                                 // query heads per kv head
 constexpr int kStages = 3;
-constexpr int kConsumerWarps = 4;
-constexpr int kConsumers = kConsumerWarps * 32;
-constexpr int kThreads = kConsumers + 32;                // + one producer warp
+constexpr int kGroups = 4;                               // 16-token groups per page
 constexpr int kBoxCols = 64;                             // 128 B swizzle span
 constexpr int kBoxBytes = kPage * kBoxCols * 2;          // 8 KiB
 constexpr int kHalfBytes = kBoxBytes * (kD / kBoxCols);  // K (or V) slice: 32 KiB
 constexpr int kStageBytes = 2 * kHalfBytes;              // 64 KiB
 constexpr int kXRow = kD + 8;                            // padded exchange row
-constexpr int kXOBytes = kConsumerWarps * kMaxG * kXRow * 4;
-constexpr int kXMLBytes = kConsumerWarps * kMaxG * 2 * 4;
+constexpr int kXOBytes = kGroups * kMaxG * kXRow * 4;
+constexpr int kXMLBytes = kGroups * kMaxG * 2 * 4;
 constexpr int kSmemXO = kStages * kStageBytes;
 constexpr int kSmemXML = kSmemXO + kXOBytes;
 constexpr int kSmemBar = kSmemXML + kXMLBytes;
@@ -73,9 +76,13 @@ constexpr size_t kStatusBytes = 256;
 constexpr size_t kCounterBytes = 4 * kMaxUnitsLarge;
 constexpr size_t kPartOBytes = size_t(kMaxG) * kD * 4;   // per partial slot
 constexpr size_t kPartMLBytes = size_t(kMaxG) * 2 * 4;
-constexpr float kLn2 = 0.693147180559945309f;
+constexpr double kLn2 = 0.693147180559945309;
 constexpr float kLog2e = 1.44269504088896341f;
-constexpr float kRescaleThreshold = 8.0f;                // log2 units
+// The running softmax reference is kept on multiples of kRefStep (log2 units):
+// rescales and the weights between partials are then exact powers of two, and
+// every probability is the same number (up to an exact power of two) however
+// the tokens are split into tiles, chunks and warps.
+constexpr float kRefStep = 8.0f;
 
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
 
@@ -135,10 +142,27 @@ __device__ __forceinline__ int first_unit(const Params<N>& p, long long start) {
   return ans;
 }
 
+// ln-domain LSE of a reference m (log2 units, a multiple of kRefStep) and a
+// sum l: m ln 2 + ln l, evaluated in double and rounded once to fp32, so the
+// LSE a tile hands to the merge carries only its own fp32 rounding.
+__device__ __forceinline__ float lse_of(float m, float l) {
+  return static_cast<float>(static_cast<double>(m) * kLn2 + log(static_cast<double>(l)));
+}
+
+__device__ __forceinline__ float ref_ceil(float x) {
+  return ceilf(x * (1.0f / kRefStep)) * kRefStep;
+}
+
+// Weight of a partial whose reference is m relative to the common reference
+// big_m >= m (both multiples of kRefStep): exactly 2^(m - big_m), 0 for -inf.
+__device__ __forceinline__ float ref_weight(float m, float big_m) {
+  return (m == -INFINITY) ? 0.f : ptx::pow2i(static_cast<int>(m - big_m));
+}
+
 struct Shared {
   uint8_t* stages;
-  float* xo;       // [warp][kMaxG][kXRow]
-  float* xml;      // [warp][kMaxG][2]
+  float* xo;       // [token group][kMaxG][kXRow]
+  float* xml;      // [token group][kMaxG][2]
   uint32_t full_bar;
   uint32_t empty_bar;
   volatile int* poison;  // [kStages]
@@ -163,13 +187,28 @@ __device__ __forceinline__ Shared carve(uint8_t* raw) {
 }
 
 // ---------------------------------------------------------------------------
-// Per-warp accumulators of one segment (tensor-core variant).
-// o[n][0..1]: head row (lane/4), dims 8n + 2(lane%4) + {0,1}, from P_hi;
-// o[n][2..3]: the same head and dims, from P_lo.
+// Thread organisation.  Each page is split into kGroups groups of 16 tokens.
+// Tensor-core variant: 8 consumer warps; warp w takes token group w % 4 and
+// output dims [128 * (w / 4), +128): the two warps of a group compute the same
+// grouped scores (QK) and each accumulates half of P V, so every SM
+// sub-partition runs two consumer warps whose latencies overlap.
+// CUDA-core variant: 4 consumer warps, one per token group, all dims.
 // ---------------------------------------------------------------------------
+template <bool kTensorCores>
+struct Shape {
+  static constexpr int kConsumerWarps = kTensorCores ? 8 : 4;
+  static constexpr int kConsumers = kConsumerWarps * 32;
+  static constexpr int kThreads = kConsumers + 32;  // + one producer warp
+};
+constexpr int kDimHalves = 2;
+constexpr int kHalfD = kD / kDimHalves;
+
+// Tensor-core accumulators of one warp: o[n][0..1] = head row (lane/4),
+// dims 128*half + 8n + 2(lane%4) + {0,1}, from P_hi; o[n][2..3] = the same
+// head and dims, from P_lo.
 struct MmaState {
-  float o[kD / 8][4];
-  float m;  // running reference max of this lane's head row (log2 domain)
+  float o[kHalfD / 8][4];
+  float m;  // reference of this lane's head row (log2 domain, multiple of 8)
   float l;  // this lane's share of the row sum (quad-reduced at the end)
 };
 
@@ -183,9 +222,11 @@ struct FmaState {
 // The kernel.
 // ---------------------------------------------------------------------------
 template <int kMaxUnits, bool kTensorCores>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap,
                         const __grid_constant__ Params<kMaxUnits> p) {
+  constexpr int kConsumerWarps = Shape<kTensorCores>::kConsumerWarps;
+  constexpr int kConsumers = Shape<kTensorCores>::kConsumers;
   extern __shared__ uint8_t smem_raw[];
   const Shared sh = carve(smem_raw);
   const int warp = threadIdx.x >> 5;
@@ -276,8 +317,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ======================= consumer warps =======================
-  const int ct = threadIdx.x;  // 0 .. kConsumers-1
-  const int gr = lane >> 2;    // head row inside the group (tensor-core layout)
+  const int ct = threadIdx.x;      // 0 .. kConsumers-1
+  const int tg = warp % kGroups;   // token group of this warp
+  const int dh = warp / kGroups;   // dim half (tensor-core variant)
+  const int gr = lane >> 2;        // head row inside the group (tensor-core layout)
   const int tq = lane & 3;
 
   // Empty units: output 0, LSE -inf.
@@ -310,33 +353,38 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int first_page_tok = (U.tok_start / kPage) * kPage;
     int poisoned = 0;
 
-    float* xo_w = sh.xo + (warp * kMaxG) * kXRow;
-    float* xml_w = sh.xml + (warp * kMaxG) * 2;
+    float* xo_g = sh.xo + (tg * kMaxG) * kXRow;   // this token group's exchange rows
+    float* xml_g = sh.xml + (tg * kMaxG) * 2;
 
     if constexpr (kTensorCores) {
       // ---- Q fragments (A operand rows = heads; rows 8..15 stay zero) ----
-      uint32_t qa0[kD / 16], qa2[kD / 16];
+      // Staged once per segment in the exchange area (free until the
+      // publish below): qfrag[kk][lane] = {a0, a2} of k-step kk.
+      uint2* qfrag = reinterpret_cast<uint2*>(sh.xo);
       {
         const bool live = gr < G;
         const __nv_bfloat16* qrow = p.q + ((size_t)b * p.Hq + g * G + (live ? gr : 0)) * kD;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          qa0[kk] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * tq)) : 0u;
-          qa2[kk] = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * tq))
-                         : 0u;
+        for (int j = 0; j < kD / 16 / kConsumerWarps; ++j) {
+          const int kk = warp * (kD / 16 / kConsumerWarps) + j;
+          uint2 v;
+          v.x = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 2 * tq)) : 0u;
+          v.y = live ? __ldg(reinterpret_cast<const uint32_t*>(qrow + 16 * kk + 8 + 2 * tq)) : 0u;
+          qfrag[kk * 32 + lane] = v;
         }
       }
+      ptx::named_barrier(1, kConsumers);
       MmaState st;
 #pragma unroll
-      for (int n = 0; n < kD / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+      for (int n = 0; n < kHalfD / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
       st.m = -INFINITY;
       st.l = 0.f;
 
       const int r8 = lane & 7;
       const int mi = lane >> 3;
-      const uint32_t k_lane = (16 * warp + (mi >> 1) * 8 + r8) * 128;
+      const uint32_t k_lane = (16 * tg + (mi >> 1) * 8 + r8) * 128;
       const int sel_k = mi & 1;
-      const uint32_t v_lane = kHalfBytes + (16 * warp + (mi & 1) * 8 + r8) * 128;
+      const uint32_t v_lane = kHalfBytes + (16 * tg + (mi & 1) * 8 + r8) * 128;
       const int sel_v = mi >> 1;
 
       for (int lp = lo; lp < hi; ++lp, ++it) {
@@ -353,26 +401,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int page_tok = first_page_tok + lp * kPage;
         const int vlo = max(U.tok_start, page_tok);
         const int vhi = min(U.tok_end, page_tok + kPage);
-        const int tb = page_tok + 16 * warp;
+        const int tb = page_tok + 16 * tg;
         const uint32_t stage = ptx::smem_addr(sh.stages + s * kStageBytes);
         if (tb + 16 > vlo && tb < vhi) {
           if (tb < vlo || tb + 16 > vhi) {
-            // Rows of this warp outside the tile: zero their V so that a
-            // non-finite value there cannot reach the PV product.
+            // Rows of this group outside the tile: zero this warp's half of
+            // their V so that a non-finite value there cannot reach P V.
             for (int r = 0; r < 16; ++r) {
               const int tok = tb + r;
               if (tok >= vlo && tok < vhi) continue;
-              const uint32_t a = stage + kHalfBytes + (lane >> 3) * kBoxBytes +
-                                 (16 * warp + r) * 128 + (lane & 7) * 16;
-              asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u)
-                           : "memory");
+              if (lane < 16) {
+                const uint32_t a = stage + kHalfBytes + (2 * dh + (lane >> 3)) * kBoxBytes +
+                                   (16 * tg + r) * 128 + (lane & 7) * 16;
+                asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0u)
+                             : "memory");
+              }
             }
             ptx::fence_proxy_async_smem();
             __syncwarp();
           }
-          // ---- S = Q K^T for the warp's 16 tokens (two 8-token n-tiles) ----
-          float s0[4] = {0.f, 0.f, 0.f, 0.f};
-          float s1[4] = {0.f, 0.f, 0.f, 0.f};
+          // ---- S = Q K^T for the group's 16 tokens (two 8-token n-tiles) ----
+          // Even and odd k-steps accumulate separately: four independent
+          // MMA chains instead of two.
+          float s0[4] = {0.f, 0.f, 0.f, 0.f}, s0o[4] = {0.f, 0.f, 0.f, 0.f};
+          float s1[4] = {0.f, 0.f, 0.f, 0.f}, s1o[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const int chunk = 2 * kk + sel_k;
@@ -380,10 +432,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 stage + (chunk >> 3) * kBoxBytes + k_lane + (((chunk & 7) ^ r8) << 4);
             uint32_t b0, b1, b2, b3;
             ptx::ldmatrix_x4(addr, b0, b1, b2, b3);
-            ptx::mma_bf16_16816(s0, qa0[kk], 0u, qa2[kk], 0u, b0, b1);
-            ptx::mma_bf16_16816(s1, qa0[kk], 0u, qa2[kk], 0u, b2, b3);
+            const uint2 qa = qfrag[kk * 32 + lane];
+            if (kk & 1) {
+              ptx::mma_bf16_16816(s0o, qa.x, 0u, qa.y, 0u, b0, b1);
+              ptx::mma_bf16_16816(s1o, qa.x, 0u, qa.y, 0u, b2, b3);
+            } else {
+              ptx::mma_bf16_16816(s0, qa.x, 0u, qa.y, 0u, b0, b1);
+              ptx::mma_bf16_16816(s1, qa.x, 0u, qa.y, 0u, b2, b3);
+            }
           }
-          // ---- masked online softmax (log2 domain, lazy rescale) ----
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            s0[k] += s0o[k];
+            s1[k] += s1o[k];
+          }
+          // ---- masked online softmax (log2 domain, reference on multiples of 8) ----
           const bool live = gr < G;
           const int j0 = tb + 2 * tq;
           float x[4];
@@ -394,12 +457,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           float bm = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
           bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 1));
           bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, 2));
-          const bool need = bm > st.m + kRescaleThreshold;
+          const bool need = bm > st.m;
           if (__any_sync(0xffffffffu, need)) {
-            const float m_new = fmaxf(st.m, bm);
-            const float alpha = (st.m == -INFINITY) ? 0.f : exp2f(st.m - m_new);
+            const float m_new = fmaxf(st.m, ref_ceil(bm));
+            const float alpha = ref_weight(st.m, m_new);
 #pragma unroll
-            for (int n = 0; n < kD / 8; ++n) {
+            for (int n = 0; n < kHalfD / 8; ++n) {
               st.o[n][0] *= alpha;
               st.o[n][1] *= alpha;
               st.o[n][2] *= alpha;
@@ -411,7 +474,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float mu = (st.m == -INFINITY) ? 0.f : st.m;
           float pr[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) pr[k] = exp2f(x[k] - mu);
+          for (int k = 0; k < 4; ++k) pr[k] = ptx::ex2(x[k] - mu);
           st.l += (pr[0] + pr[1]) + (pr[2] + pr[3]);
           __nv_bfloat16 ph[4], pl[4];
 #pragma unroll
@@ -423,34 +486,45 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t pa1 = ptx::pack_bf16x2(pl[0], pl[1]);
           const uint32_t pa2 = ptx::pack_bf16x2(ph[2], ph[3]);
           const uint32_t pa3 = ptx::pack_bf16x2(pl[2], pl[3]);
-          // ---- O += P V ----
+          // ---- O += P V over this warp's dim half ----
+          // Each page's product starts from a zero accumulator and is added
+          // to O in fp32 with round-to-nearest, so the long running sum does
+          // not inherit the tensor core's accumulation rounding.
 #pragma unroll
-          for (int nd2 = 0; nd2 < kD / 16; ++nd2) {
-            const int chunk = 2 * nd2 + sel_v;
+          for (int nd2 = 0; nd2 < kHalfD / 16; ++nd2) {
+            const int chunk = (kHalfD / 8) * dh + 2 * nd2 + sel_v;
             const uint32_t addr =
                 stage + (chunk >> 3) * kBoxBytes + v_lane + (((chunk & 7) ^ r8) << 4);
             uint32_t b0, b1, b2, b3;
             ptx::ldmatrix_x4_trans(addr, b0, b1, b2, b3);
-            ptx::mma_bf16_16816(st.o[2 * nd2], pa0, pa1, pa2, pa3, b0, b1);
-            ptx::mma_bf16_16816(st.o[2 * nd2 + 1], pa0, pa1, pa2, pa3, b2, b3);
+            float t0[4] = {0.f, 0.f, 0.f, 0.f};
+            float t1[4] = {0.f, 0.f, 0.f, 0.f};
+            ptx::mma_bf16_16816(t0, pa0, pa1, pa2, pa3, b0, b1);
+            ptx::mma_bf16_16816(t1, pa0, pa1, pa2, pa3, b2, b3);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              st.o[2 * nd2][k] += t0[k];
+              st.o[2 * nd2 + 1][k] += t1[k];
+            }
           }
         }
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(sh.empty_bar + 8 * s);
       }
       // ---- publish this warp's state for the CTA-level combine ----
+      ptx::named_barrier(1, kConsumers);  // every warp is done with qfrag
       st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
       st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
       if (gr < G) {
-        float* row = xo_w + gr * kXRow;
+        float* row = xo_g + gr * kXRow + kHalfD * dh;
 #pragma unroll
-        for (int n = 0; n < kD / 8; ++n) {
+        for (int n = 0; n < kHalfD / 8; ++n) {
           *reinterpret_cast<float2*>(row + 8 * n + 2 * tq) =
               make_float2(st.o[n][0] + st.o[n][2], st.o[n][1] + st.o[n][3]);
         }
-        if (tq == 0) {
-          xml_w[gr * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m;
-          xml_w[gr * 2 + 1] = st.l;
+        if (tq == 0 && dh == 0) {
+          xml_g[gr * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m;
+          xml_g[gr * 2 + 1] = st.l;
         }
       }
     } else {
@@ -493,12 +567,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int page_tok = first_page_tok + lp * kPage;
         const int vlo = max(U.tok_start, page_tok);
         const int vhi = min(U.tok_end, page_tok + kPage);
-        const int tb = page_tok + 16 * warp;
+        const int tb = page_tok + 16 * tg;
         const uint32_t stage = ptx::smem_addr(sh.stages + s * kStageBytes);
         const int r_lo = max(0, vlo - tb);
         const int r_hi = min(16, vhi - tb);
         for (int r = r_lo; r < r_hi; ++r) {
-          const int row = 16 * warp + r;
+          const int row = 16 * tg + r;
           const uint32_t ka = stage + lane_box + row * 128 + ((lane_chunk ^ (row & 7)) << 4);
           uint32_t k4[4], v4[4];
           asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -532,13 +606,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int h = 0; h < kMaxG; ++h) {
             x[h] = h < G ? x[h] * p.scale_log2 : -INFINITY;
-            need |= x[h] > st.m[h] + kRescaleThreshold;
+            need |= x[h] > st.m[h];
           }
           if (need) {  // uniform: every lane holds the same reduced scores
 #pragma unroll
             for (int h = 0; h < kMaxG; ++h) {
-              const float m_new = fmaxf(st.m[h], x[h]);
-              const float alpha = (st.m[h] == -INFINITY) ? 0.f : exp2f(st.m[h] - m_new);
+              const float m_new = fmaxf(st.m[h], ref_ceil(x[h]));
+              const float alpha = ref_weight(st.m[h], m_new);
 #pragma unroll
               for (int i = 0; i < 8; ++i) st.o[h][i] *= alpha;
               st.l[h] *= alpha;
@@ -547,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
 #pragma unroll
           for (int h = 0; h < kMaxG; ++h) {
-            const float pr = exp2f(x[h] - (st.m[h] == -INFINITY ? 0.f : st.m[h]));
+            const float pr = ptx::ex2(x[h] - (st.m[h] == -INFINITY ? 0.f : st.m[h]));
             st.l[h] += pr;
 #pragma unroll
             for (int i = 0; i < 8; ++i) st.o[h][i] = fmaf(pr, vf[i], st.o[h][i]);
@@ -559,20 +633,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int h = 0; h < kMaxG; ++h) {
         if (h < G) {
-          float* row = xo_w + h * kXRow + 8 * lane;
+          float* row = xo_g + h * kXRow + 8 * lane;
           *reinterpret_cast<float4*>(row) =
               make_float4(st.o[h][0], st.o[h][1], st.o[h][2], st.o[h][3]);
           *reinterpret_cast<float4*>(row + 4) =
               make_float4(st.o[h][4], st.o[h][5], st.o[h][6], st.o[h][7]);
           if (lane == 0) {
-            xml_w[h * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m[h];
-            xml_w[h * 2 + 1] = st.l[h];
+            xml_g[h * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m[h];
+            xml_g[h * 2 + 1] = st.l[h];
           }
         }
       }
     }
 
-    // ================= CTA-level combine of the 4 warps =================
+    // ============ CTA-level combine of the kGroups token groups ============
     ptx::named_barrier(1, kConsumers);
     if (!ok || *sh.abort_flag) {
       ok = false;
@@ -584,19 +658,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int idx = ct; idx < G * kD; idx += kConsumers) {
       const int row = idx / kD;
       const int d = idx - row * kD;
-      float mw[kConsumerWarps];
+      float mw[kGroups];
       float big_m = -INFINITY;
       bool nan = false;
 #pragma unroll
-      for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
+      for (int w2 = 0; w2 < kGroups; ++w2) {
         mw[w2] = sh.xml[(w2 * kMaxG + row) * 2];
         nan |= (mw[w2] != mw[w2]);
         big_m = fmaxf(big_m, mw[w2]);
       }
       float o = 0.f, l = 0.f;
 #pragma unroll
-      for (int w2 = 0; w2 < kConsumerWarps; ++w2) {
-        const float a = (mw[w2] == -INFINITY) ? 0.f : exp2f(mw[w2] - big_m);
+      for (int w2 = 0; w2 < kGroups; ++w2) {
+        const float a = ref_weight(mw[w2], big_m);
         o = fmaf(a, sh.xo[(w2 * kMaxG + row) * kXRow + d], o);
         l = fmaf(a, sh.xml[(w2 * kMaxG + row) * 2 + 1], l);
       }
@@ -604,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (single) {
         const size_t orow = (size_t)bt * p.Hq + g * G + row;
         p.out[orow * kD + d] = nan ? big_m : o / l;
-        if (d == 0) p.lse[orow] = nan ? big_m : (big_m + log2f(l)) * kLn2;
+        if (d == 0) p.lse[orow] = nan ? big_m : lse_of(big_m, l);
       } else {
         p.part_o[((size_t)slot * kMaxG + row) * kD + d] = o;
         if (d == 0) {
@@ -623,44 +697,84 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ptx::named_barrier(1, kConsumers);
       if (*sh.merge_flag) {
+        // One CTA finishes the unit while the rest of the grid is idle, so
+        // this is latency-bound: every thread issues all of its loads before
+        // it does any arithmetic (one L2 round trip per phase).
         __threadfence();
+        const int n = U.n_parts;
         float* wts = sh.xo;                 // [part][kMaxG]
         float* row_l = sh.xml;              // [kMaxG]
         float* row_m = sh.xml + kMaxG;      // [kMaxG]
-        if (ct < G) {
-          const int row = ct;
-          float big_m = -INFINITY;
-          bool nan = false;
-          for (int c = 0; c < U.n_parts; ++c) {
-            const float mc = __ldcg(p.part_ml + ((size_t)(U.part_base + c) * kMaxG + row) * 2);
+        const float2* pml = reinterpret_cast<const float2*>(p.part_ml) +
+                            (size_t)U.part_base * kMaxG;
+        for (int row = warp; row < G; row += kConsumerWarps) {
+          const float2 first =
+              lane < n ? __ldcg(pml + (size_t)lane * kMaxG + row) : make_float2(-INFINITY, 0.f);
+          float big_m = first.x;
+          int nan = (first.x != first.x);
+          for (int c = lane + 32; c < n; c += 32) {
+            const float mc = __ldcg(pml + (size_t)c * kMaxG + row).x;
             nan |= (mc != mc);
             big_m = fmaxf(big_m, mc);
           }
-          float l = 0.f;
-          for (int c = 0; c < U.n_parts; ++c) {
-            const float* ml = p.part_ml + ((size_t)(U.part_base + c) * kMaxG + row) * 2;
-            const float mc = __ldcg(ml);
-            const float a = (mc == -INFINITY) ? 0.f : exp2f(mc - big_m);
-            wts[c * kMaxG + row] = a;
-            l = fmaf(a, __ldcg(ml + 1), l);
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, off));
+            nan |= __shfl_xor_sync(0xffffffffu, nan, off);
           }
-          row_l[row] = l;
-          row_m[row] = nan ? __int_as_float(0x7fc00000) : big_m;
+          float l = 0.f;
+          if (lane < n) {
+            const float a = ref_weight(first.x, big_m);
+            wts[lane * kMaxG + row] = a;
+            l = a * first.y;
+          }
+          for (int c = lane + 32; c < n; c += 32) {
+            const float2 ml = __ldcg(pml + (size_t)c * kMaxG + row);
+            const float a = ref_weight(ml.x, big_m);
+            wts[c * kMaxG + row] = a;
+            l = fmaf(a, ml.y, l);
+          }
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
+          if (lane == 0) {
+            row_l[row] = l;
+            row_m[row] = nan ? __int_as_float(0x7fc00000) : big_m;
+          }
         }
         ptx::named_barrier(1, kConsumers);
-        for (int idx = ct; idx < G * kD; idx += kConsumers) {
-          const int row = idx / kD;
-          const int d = idx - row * kD;
-          float o = 0.f;
-          for (int c = 0; c < U.n_parts; ++c) {
-            o = fmaf(wts[c * kMaxG + row],
-                     __ldcg(p.part_o + ((size_t)(U.part_base + c) * kMaxG + row) * kD + d), o);
+        constexpr int kVec = kD / 4;        // float4 per output row
+        constexpr int kBatch = kTensorCores ? 16 : 8;  // register headroom differs
+        constexpr size_t kPartStride = (size_t)kMaxG * kVec;
+        const float4* po =
+            reinterpret_cast<const float4*>(p.part_o) + (size_t)U.part_base * kPartStride;
+        for (int idx = ct; idx < G * kVec; idx += kConsumers) {
+          const int row = idx / kVec;
+          const int dv = idx - row * kVec;
+          const float4* src = po + (size_t)row * kVec + dv;
+          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+          for (int c = 0; c < n; c += kBatch) {
+            // Past the last partial, reload the last one with weight 0.
+            float4 v[kBatch];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k)
+              v[k] = __ldcg(src + (size_t)min(c + k, n - 1) * kPartStride);
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const float a = (c + k < n) ? wts[min(c + k, n - 1) * kMaxG + row] : 0.f;
+              acc.x = fmaf(a, v[k].x, acc.x);
+              acc.y = fmaf(a, v[k].y, acc.y);
+              acc.z = fmaf(a, v[k].z, acc.z);
+              acc.w = fmaf(a, v[k].w, acc.w);
+            }
           }
           const float big_m = row_m[row];
           const bool nan = big_m != big_m;
+          const float rl = row_l[row];
           const size_t orow = (size_t)bt * p.Hq + g * G + row;
-          p.out[orow * kD + d] = nan ? big_m : o / row_l[row];
-          if (d == 0) p.lse[orow] = nan ? big_m : (big_m + log2f(row_l[row])) * kLn2;
+          reinterpret_cast<float4*>(p.out + orow * kD)[dv] =
+              nan ? make_float4(big_m, big_m, big_m, big_m)
+                  : make_float4(acc.x / rl, acc.y / rl, acc.z / rl, acc.w / rl);
+          if (dv == 0) p.lse[orow] = nan ? big_m : lse_of(big_m, rl);
         }
         if (ct == 0) p.counters[u] = 0;
       }
@@ -716,7 +830,7 @@ cudaError_t launch(const CUtensorMap& tmap, const Params<N>& prm, int grid, cuda
       configured[dev] = true;
     }
   }
-  paged_decode_kernel<N, TC><<<grid, kThreads, kSmemAlloc, stream>>>(tmap, prm);
+  paged_decode_kernel<N, TC><<<grid, Shape<TC>::kThreads, kSmemAlloc, stream>>>(tmap, prm);
   return cudaGetLastError();
 }
 
@@ -758,6 +872,7 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
   PA_REQUIRE(max_pages >= 1 && pool_pages >= 1, "max_pages and pool_pages must be >= 1");
   PA_REQUIRE(reinterpret_cast<uintptr_t>(q) % 16 == 0, "q must be 16-byte aligned");
   PA_REQUIRE(reinterpret_cast<uintptr_t>(pool) % 16 == 0, "pool must be 16-byte aligned");
+  PA_REQUIRE(reinterpret_cast<uintptr_t>(out) % 16 == 0, "out must be 16-byte aligned");
   PA_REQUIRE(reinterpret_cast<uintptr_t>(workspace) % 256 == 0,
              "workspace must be 256-byte aligned");
   PA_REQUIRE(pool_pages * kPage < (1ll << 31), "pool too large for 32-bit row coordinates");

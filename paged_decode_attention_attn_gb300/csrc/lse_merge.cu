@@ -85,7 +85,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     }
     wsum = ws;
   }
-  if (lane == 0) lse[(size_t)b * H + h] = big_m + logf(wsum);
+  if (lane == 0) lse[(size_t)b * H + h] =
+        static_cast<float>(static_cast<double>(big_m) + log(static_cast<double>(wsum)));
 }
 
 // One warp per row: copy rows[b] into the pool row of token positions[b].

@@ -113,12 +113,20 @@ def test_physical_placement_does_not_change_bits(B, D, cuda_core):
     assert torch.equal(a.o.out, b.o.out) and torch.equal(a.o.lse, b.o.lse)
 
 
+# The tensor-core kernel carries each probability as a bf16 hi + lo pair
+# (relative error <= 2^-18); the CUDA-core kernel keeps fp32.  Their outputs
+# can differ by up to 2^-18 * max|v - out| (~4e-6 * 10 for N(0,1) values), so
+# the two are held to 1e-4 here, well inside the 2e-3 bound both meet against
+# the oracle.  LSEs do not depend on that rounding.
+TOL_VARIANTS_OUT = 1e-4
+
+
 def test_variants_agree(B, D):
     w = edge_workload()
     t = wl.materialize(w, "cuda")
     a = run_resident(D, w, t, False)
     b = run_resident(D, w, t, True)
-    assert max_abs(a.o.out.cpu(), b.o.out.cpu()) <= 2 * TOL_SPLIT
+    assert max_abs(a.o.out.cpu(), b.o.out.cpu()) <= TOL_VARIANTS_OUT
     assert max_abs(a.o.lse.cpu(), b.o.lse.cpu()) <= 2 * TOL_SPLIT
 
 
