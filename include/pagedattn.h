@@ -139,6 +139,37 @@ int paged_decode_attn_lse_cuda_core(const void* q, const void* pool, int64_t poo
                                     void* workspace, size_t workspace_bytes,
                                     cudaStream_t stream);
 
+/* The same computation as paged_decode_attn_lse (tensor-core kernel), for
+ * callers that cannot allocate device memory: there is no workspace argument.
+ * The source pages have no counterpart to this entry point.
+ *
+ * Who needs it: code that fixes its device-memory budget before it starts
+ * serving and forbids allocation afterwards, or that cannot pay for
+ * cudaMalloc's possible device-wide synchronisation in its hot loop, and so
+ * cannot hand this library a workspace.  The scratch instead lives in a fixed
+ * array of PA_NOALLOC_SCRATCH_BYTES (16 MiB) among the library's device
+ * globals, which every GPU that loads the library keeps until the process
+ * exits.  Nothing here calls cudaMalloc, cudaFree or an allocating routine.
+ *
+ *   All arguments as for paged_decode_attn_lse, except:
+ *   status  optional device int32; receives the call's PA_STATUS_* bits (the
+ *           copy is enqueued on the stream after the kernel), or NULL.
+ * Returns PA_ERR_INVALID, before touching the GPU, when the call would need
+ * more scratch than the array holds (above ~1,000 (request, tile, kv head)
+ * units); paged_decode_attn_lse with a caller workspace has no such limit.
+ * The first call on each device looks up the array's device address with
+ * that device current; make that first call before any stream capture.  Every
+ * call clears the start of the array and reuses the rest, so calls whose
+ * kernels may overlap on the GPU (unordered streams) race and must not be
+ * issued. */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int paged_decode_attn_lse_noalloc(const void* q, const void* pool, int64_t pool_pages,
+                                  const int32_t* page_table, int max_pages,
+                                  const int32_t* tiles, int B, int T,
+                                  int n_q_heads, int n_kv_heads, int head_dim,
+                                  float scale, float* out, float* lse,
+                                  int32_t* status, cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* FP32 LSE merge  ([KVE-exact])                                            */
 /* ------------------------------------------------------------------------ */

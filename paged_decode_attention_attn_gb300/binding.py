@@ -33,7 +33,8 @@ PAGE_TOKENS = 64
 EXPORTED = [
     "kv_last_error", "pa_version",
     "paged_decode_attn_lse_workspace_bytes", "paged_decode_attn_lse",
-    "paged_decode_attn_lse_cuda_core", "lse_merge", "kv_append_rows",
+    "paged_decode_attn_lse_cuda_core", "paged_decode_attn_lse_noalloc", "lse_merge",
+    "kv_append_rows",
     "kv_arena_create", "kv_arena_destroy", "kv_arena_drain", "kv_stage_layer",
     "kv_mark_attention_done", "kv_writeback_tail", "kv_arena_get_stats",
     "kv_arena_fail_after", "kv_arena_call_log",
@@ -122,6 +123,9 @@ def _load():
     for name in ("paged_decode_attn_lse", "paged_decode_attn_lse_cuda_core"):
         getattr(lib, name).restype = i32
         getattr(lib, name).argtypes = dec
+    lib.paged_decode_attn_lse_noalloc.restype = i32
+    lib.paged_decode_attn_lse_noalloc.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32,
+                                                  i32, ctypes.c_float, vp, vp, vp, vp]
     lib.lse_merge.restype = i32
     lib.lse_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
     lib.kv_append_rows.restype = i32
@@ -215,6 +219,29 @@ def paged_decode_attn_lse(q, pool, page_table, tiles, scale, out, lse, workspace
               _dev(out, torch.float32, "out"), _dev(lse, torch.float32, "lse"),
               _dev(workspace, torch.uint8, "workspace"), workspace.numel(),
               _stream_handle(stream)))
+
+
+def paged_decode_attn_lse_noalloc(q, pool, page_table, tiles, scale, out, lse, status=None,
+                                  stream=None, pool_pages=None):
+    """Same as paged_decode_attn_lse without a workspace argument: for callers
+    that cannot allocate device memory, the library uses its own fixed device
+    scratch array.  ``status`` (optional int32 CUDA tensor of 1 element)
+    receives the call's status bits."""
+    Bn, Hq, D = q.shape
+    row_elems = pool.shape[-1]
+    n_kv = row_elems // (2 * D)
+    arr, tiles_ptr = _host_tiles(tiles)
+    T = arr.shape[1]
+    if arr.shape[0] != Bn:
+        raise ValueError("tiles must be [B][T][2]")
+    if pool_pages is None:
+        pool_pages = pool.numel() // (PAGE_TOKENS * row_elems)
+    _check(lib.paged_decode_attn_lse_noalloc(
+        _dev(q, torch.bfloat16, "q"), _dev(pool, torch.bfloat16, "pool", False), int(pool_pages),
+        _dev(page_table, torch.int32, "page_table"), int(page_table.shape[1]), tiles_ptr, Bn, T,
+        Hq, n_kv, D, float(scale), _dev(out, torch.float32, "out"),
+        _dev(lse, torch.float32, "lse"),
+        None if status is None else _dev(status, torch.int32, "status"), _stream_handle(stream)))
 
 
 def lse_merge(out_parts, lse_parts, part_offsets, out, lse, stream=None):

@@ -1018,3 +1018,87 @@ extern "C" int paged_decode_attn_lse_cuda_core(const void* q, const void* pool,
                          n_q_heads, n_kv_heads, head_dim, scale, out, lse, workspace,
                          workspace_bytes, stream);
 }
+
+// ---------------------------------------------------------------------------
+// Decode attention for callers that cannot allocate device memory.
+//
+// Some callers fix their device-memory budget before they start serving and
+// forbid any allocation afterwards (so a long-running process cannot grow or
+// fragment its footprint), and some cannot afford cudaMalloc in their hot
+// loop because it can synchronise the whole device.  They cannot provide the
+// workspace paged_decode_attn_lse asks for, so this entry point brings its
+// own: a fixed array in this library's device globals, which every GPU that
+// loads the library holds until the process exits.  The array is shared by
+// every call on a device and keeps the previous call's contents; each call
+// clears the part that must start at zero.  Calls that can overlap on the GPU
+// (on different streams without ordering) race on the array.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_ptr[64] = {nullptr};
+
+// Device address of the scratch array on the current device.  The host-side
+// name of the array is not a device address; the runtime is asked for it once
+// per device, with that device current.
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return pa::fail(PA_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= 64) return pa::fail(PA_ERR_INVALID, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (g_noalloc_ptr[dev] == nullptr) {
+    void* ptr = nullptr;
+    const cudaError_t r = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
+    if (r != cudaSuccess || ptr == nullptr)
+      return pa::fail(PA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s",
+                      cudaGetErrorString(r));
+    g_noalloc_ptr[dev] = ptr;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PA_OK;
+}
+
+}  // namespace
+
+extern "C" int paged_decode_attn_lse_noalloc(const void* q, const void* pool, int64_t pool_pages,
+                                             const int32_t* page_table, int max_pages,
+                                             const int32_t* tiles, int B, int T, int n_q_heads,
+                                             int n_kv_heads, int head_dim, float scale,
+                                             float* out, float* lse, int32_t* status,
+                                             cudaStream_t stream) {
+  pa::clear_error();
+  if (B < 0 || T < 0) return pa::fail(PA_ERR_INVALID, "B and T must be >= 0 (got %d, %d)", B, T);
+  if ((long long)B * T == 0) return PA_OK;
+  const size_t need =
+      paged_decode_attn_lse_workspace_bytes(B, T, n_q_heads, n_kv_heads, head_dim);
+  if (need > kNoAllocScratchBytes)
+    return pa::fail(PA_ERR_INVALID,
+                    "this call needs %zu bytes of scratch, more than the %zu bytes the "
+                    "no-allocation entry point holds; pass a workspace to "
+                    "paged_decode_attn_lse instead",
+                    need, kNoAllocScratchBytes);
+  void* scratch = nullptr;
+  int rc = noalloc_scratch(&scratch);
+  if (rc != PA_OK) return rc;
+  // Status word and arrival counters must start at zero.
+  const cudaError_t e = cudaMemsetAsync(scratch, 0, pa::decode::kStatusBytes + pa::decode::kCounterBytes,
+                                        stream);
+  if (e != cudaSuccess)
+    return pa::fail(PA_ERR_CUDA, "clearing the scratch array failed: %s", cudaGetErrorString(e));
+  rc = pa::decode::run(true, q, pool, pool_pages, page_table, max_pages, tiles, B, T, n_q_heads,
+                       n_kv_heads, head_dim, scale, out, lse, scratch, kNoAllocScratchBytes,
+                       stream);
+  if (rc != PA_OK) return rc;
+  if (status != nullptr) {
+    const cudaError_t c =
+        cudaMemcpyAsync(status, scratch, sizeof(int32_t), cudaMemcpyDeviceToDevice, stream);
+    if (c != cudaSuccess)
+      return pa::fail(PA_ERR_CUDA, "copying the status word failed: %s", cudaGetErrorString(c));
+  }
+  return PA_OK;
+}
