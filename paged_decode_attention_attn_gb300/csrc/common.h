@@ -16,6 +16,25 @@ void clear_error();
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
+// Launches a kernel that may start while the previous kernel in the stream is
+// still running (programmatic dependent launch).  The kernel must execute
+// griddepcontrol.wait before it reads anything the previous kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 }  // namespace pa
 
 #define PA_CHECK_CUDA(call)                                                    \

@@ -244,7 +244,11 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     *sh.merge_flag = 0;
     ptx::mbar_init_fence();
   }
+  if (warp == kConsumerWarps && lane == 0) ptx::prefetch_tensormap(&tmap);
   __syncthreads();
+  // Everything above touches only parameters and shared memory; from here on
+  // the kernel reads what earlier kernels in the stream wrote.
+  ptx::grid_dependency_wait();
 
   const long long cta_start = (long long)blockIdx.x * p.total_pages / p.grid;
   const long long cta_end = (long long)(blockIdx.x + 1) * p.total_pages / p.grid;
@@ -307,6 +311,9 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         }
       }
     }
+    // Every page of this CTA is requested: the next kernel in the stream may
+    // start its prologue (it waits for this grid before reading our output).
+    if (lane == 0) ptx::launch_dependents();
     if (!ok && lane == 0) {
       // Let the copies already issued land before the CTA can exit.
       for (int k = max(0, it - kStages); k < it; ++k) {
@@ -830,7 +837,9 @@ cudaError_t launch(const CUtensorMap& tmap, const Params<N>& prm, int grid, cuda
       configured[dev] = true;
     }
   }
-  paged_decode_kernel<N, TC><<<grid, Shape<TC>::kThreads, kSmemAlloc, stream>>>(tmap, prm);
+  e = launch_dependent(paged_decode_kernel<N, TC>, dim3(grid), dim3(Shape<TC>::kThreads),
+                       kSmemAlloc, stream, tmap, prm);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -13,6 +13,7 @@
 #include <cmath>
 
 #include "common.h"
+#include "ptx.cuh"
 
 namespace pa {
 namespace merge {
@@ -24,6 +25,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     lse_merge_kernel(const float* __restrict__ out_parts, const float* __restrict__ lse_parts,
                      const int32_t* __restrict__ offsets, int B, int H, int D,
                      float* __restrict__ out, float* __restrict__ lse) {
+  ptx::launch_dependents();
+  ptx::grid_dependency_wait();  // the partials come from the previous kernel
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (wid >= (long long)B * H) return;
@@ -95,6 +98,8 @@ __global__ void append_rows_kernel(uint8_t* __restrict__ pool, long long pool_pa
                                    const int32_t* __restrict__ positions,
                                    const uint8_t* __restrict__ rows, int B, int row_bytes,
                                    int32_t* status) {
+  ptx::launch_dependents();
+  ptx::grid_dependency_wait();  // earlier kernels may still read this row's page
   const int lane = threadIdx.x & 31;
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (b >= B) return;
@@ -133,8 +138,9 @@ extern "C" int lse_merge(const float* out_parts, const float* lse_parts,
   const long long warps = (long long)B * H;
   const long long blocks = (warps + pa::merge::kWarpsPerBlock - 1) / pa::merge::kWarpsPerBlock;
   PA_REQUIRE(blocks < (1ll << 31), "too many (request, head) pairs");
-  pa::merge::lse_merge_kernel<<<(unsigned)blocks, pa::merge::kWarpsPerBlock * 32, 0, stream>>>(
-      out_parts, lse_parts, part_offsets, B, H, D, out, lse);
+  PA_CHECK_CUDA(pa::launch_dependent(pa::merge::lse_merge_kernel, dim3((unsigned)blocks),
+                                     dim3(pa::merge::kWarpsPerBlock * 32), 0, stream, out_parts,
+                                     lse_parts, part_offsets, B, H, D, out, lse));
   PA_CHECK_CUDA(cudaGetLastError());
   return PA_OK;
 }
@@ -152,9 +158,11 @@ extern "C" int kv_append_rows(void* pool, int64_t pool_pages, const int32_t* pag
              "pool and rows must be 16-byte aligned");
   const int warps_per_block = 4;
   const int blocks = (B + warps_per_block - 1) / warps_per_block;
-  pa::merge::append_rows_kernel<<<blocks, warps_per_block * 32, 0, stream>>>(
-      static_cast<uint8_t*>(pool), pool_pages, page_table, max_pages, positions,
-      static_cast<const uint8_t*>(rows), B, row_bytes, status);
+  PA_CHECK_CUDA(pa::launch_dependent(pa::merge::append_rows_kernel, dim3(blocks),
+                                     dim3(warps_per_block * 32), 0, stream,
+                                     static_cast<uint8_t*>(pool), pool_pages, page_table,
+                                     max_pages, positions, static_cast<const uint8_t*>(rows), B,
+                                     row_bytes, status));
   PA_CHECK_CUDA(cudaGetLastError());
   return PA_OK;
 }
