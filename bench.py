@@ -60,6 +60,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-workers", type=int, default=0)
+    ap.add_argument("--bus-model", action="store_true",
+                    help="fit the staged route's latency model over 32K-262K tokens "
+                         "(prints its own JSON line instead of the bench line)")
     return ap.parse_args()
 
 
@@ -489,8 +492,58 @@ def run_e2e(args, w, t, dev, D, B):
     return res
 
 
+def run_bus_model(args):
+    """Staged-route step time at 32K, 64K, 128K and 262K tokens (1 request,
+    all layers), fitted as t = fixed + bytes / bandwidth."""
+    import torch
+    from paged_decode_attention_attn_gb300 import busmodel as bm
+    from paged_decode_attention_attn_gb300 import decode as D
+    from paged_decode_attention_attn_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    points, rows = [], []
+    for L in (32768, 65536, 131072, 262144):
+        w = wl.custom([L], [[(0, L)]], seed=31, n_layers=args.layers, n_spare=2)
+        t = wl.materialize(w, dev)
+        host = D.HostHistory(w, t)
+        st = D.StagedDecode(w, t, host, n_slots=2)
+        for _ in range(2):
+            st.step()
+        st.drain()
+        torch.cuda.synchronize(dev)
+        n = 5
+        t0 = time.perf_counter()
+        for _ in range(n):
+            st.step()
+        st.drain()
+        torch.cuda.synchronize(dev)
+        secs = (time.perf_counter() - t0) / n
+        stats = st.handle.stats()
+        staged = stats.staged_bytes // stats.stage_generation * w.n_layers
+        points.append((staged, secs))
+        rows.append({"ctx": L, "staged_bytes": int(staged), "step_ms": round(1e3 * secs, 3)})
+        st.close()
+        host.close()
+        del st, host, t
+        torch.cuda.empty_cache()
+    model = bm.fit(points)
+    ends = bm.fit([points[0], points[-1]])
+    for r, e in zip(rows, bm.relative_errors(model, points)):
+        r["fit_error_pct"] = round(100 * e, 3)
+    print(json.dumps({
+        "bus_model": {k: round(v, 4) for k, v in model.as_dict().items()},
+        "worst_error_pct": round(100 * bm.worst_relative_error(model, points), 3),
+        "endpoint_model": {k: round(v, 4) for k, v in ends.as_dict().items()},
+        "endpoint_model_worst_error_pct":
+            round(100 * bm.worst_relative_error(ends, points), 3),
+        "points": rows, "layers": args.layers, "route": "host-staged, 2 arena slots"}),
+        flush=True)
+
+
 def main():
     args = parse_args()
+    if args.bus_model:
+        run_bus_model(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

@@ -61,7 +61,7 @@ constexpr int kHalfBytes = kBoxBytes * (kD / kBoxCols);  // K (or V) slice: 32 K
 constexpr int kStageBytes = 2 * kHalfBytes;              // 64 KiB
 constexpr int kXRow = kD + 8;                            // padded exchange row
 constexpr int kXOBytes = kGroups * kMaxG * kXRow * 4;
-constexpr int kXMLBytes = kGroups * kMaxG * 2 * 4;
+constexpr int kXMLBytes = kGroups * kMaxG * 2 * 4;  // >= 3 * kMaxG floats for the merge
 constexpr int kSmemXO = kStages * kStageBytes;
 constexpr int kSmemXML = kSmemXO + kXOBytes;
 constexpr int kSmemBar = kSmemXML + kXMLBytes;
@@ -712,6 +712,7 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         float* wts = sh.xo;                 // [part][kMaxG]
         float* row_l = sh.xml;              // [kMaxG]
         float* row_m = sh.xml + kMaxG;      // [kMaxG]
+        float* row_lse = sh.xml + 2 * kMaxG;  // [kMaxG]
         const float2* pml = reinterpret_cast<const float2*>(p.part_ml) +
                             (size_t)U.part_base * kMaxG;
         for (int row = warp; row < G; row += kConsumerWarps) {
@@ -744,44 +745,73 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
 #pragma unroll
           for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
           if (lane == 0) {
+            const float m_out = nan ? __int_as_float(0x7fc00000) : big_m;
             row_l[row] = l;
-            row_m[row] = nan ? __int_as_float(0x7fc00000) : big_m;
+            row_m[row] = m_out;
+            row_lse[row] = nan ? m_out : lse_of(big_m, l);
           }
         }
         ptx::named_barrier(1, kConsumers);
+        // Each thread owns up to two float4 outputs and issues the loads of
+        // both (kBatch partials each) before any arithmetic.
         constexpr int kVec = kD / 4;        // float4 per output row
-        constexpr int kBatch = kTensorCores ? 16 : 8;  // register headroom differs
+        constexpr int kBatch = kTensorCores ? 12 : 6;  // register headroom differs
         constexpr size_t kPartStride = (size_t)kMaxG * kVec;
         const float4* po =
             reinterpret_cast<const float4*>(p.part_o) + (size_t)U.part_base * kPartStride;
-        for (int idx = ct; idx < G * kVec; idx += kConsumers) {
-          const int row = idx / kVec;
-          const int dv = idx - row * kVec;
-          const float4* src = po + (size_t)row * kVec + dv;
-          float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const int n_out = G * kVec;
+        for (int base = 0; base < n_out; base += 2 * kConsumers) {
+          const int i0 = base + ct;
+          const int i1 = base + kConsumers + ct;
+          const bool h0 = i0 < n_out;
+          const bool h1 = i1 < n_out;
+          const int r0 = h0 ? i0 / kVec : 0;
+          const int r1 = h1 ? i1 / kVec : 0;
+          const float4* s0p = po + (size_t)r0 * kVec + (h0 ? i0 - r0 * kVec : 0);
+          const float4* s1p = po + (size_t)r1 * kVec + (h1 ? i1 - r1 * kVec : 0);
+          float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
+          float4 a1 = make_float4(0.f, 0.f, 0.f, 0.f);
           for (int c = 0; c < n; c += kBatch) {
             // Past the last partial, reload the last one with weight 0.
-            float4 v[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k)
-              v[k] = __ldcg(src + (size_t)min(c + k, n - 1) * kPartStride);
+            float4 v0[kBatch], v1[kBatch];
 #pragma unroll
             for (int k = 0; k < kBatch; ++k) {
-              const float a = (c + k < n) ? wts[min(c + k, n - 1) * kMaxG + row] : 0.f;
-              acc.x = fmaf(a, v[k].x, acc.x);
-              acc.y = fmaf(a, v[k].y, acc.y);
-              acc.z = fmaf(a, v[k].z, acc.z);
-              acc.w = fmaf(a, v[k].w, acc.w);
+              const size_t off = (size_t)min(c + k, n - 1) * kPartStride;
+              v0[k] = h0 ? __ldcg(s0p + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+              v1[k] = h1 ? __ldcg(s1p + off) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+              const int cc = min(c + k, n - 1);
+              const float w0 = (c + k < n) ? wts[cc * kMaxG + r0] : 0.f;
+              const float w1 = (c + k < n) ? wts[cc * kMaxG + r1] : 0.f;
+              a0.x = fmaf(w0, v0[k].x, a0.x);
+              a0.y = fmaf(w0, v0[k].y, a0.y);
+              a0.z = fmaf(w0, v0[k].z, a0.z);
+              a0.w = fmaf(w0, v0[k].w, a0.w);
+              a1.x = fmaf(w1, v1[k].x, a1.x);
+              a1.y = fmaf(w1, v1[k].y, a1.y);
+              a1.z = fmaf(w1, v1[k].z, a1.z);
+              a1.w = fmaf(w1, v1[k].w, a1.w);
             }
           }
-          const float big_m = row_m[row];
-          const bool nan = big_m != big_m;
-          const float rl = row_l[row];
-          const size_t orow = (size_t)bt * p.Hq + g * G + row;
-          reinterpret_cast<float4*>(p.out + orow * kD)[dv] =
-              nan ? make_float4(big_m, big_m, big_m, big_m)
-                  : make_float4(acc.x / rl, acc.y / rl, acc.z / rl, acc.w / rl);
-          if (dv == 0) p.lse[orow] = nan ? big_m : lse_of(big_m, rl);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const bool have = half ? h1 : h0;
+            if (!have) continue;
+            const int idx = half ? i1 : i0;
+            const int row = half ? r1 : r0;
+            const int dv = idx - row * kVec;
+            const float4 acc = half ? a1 : a0;
+            const float big_m = row_m[row];
+            const bool nan = big_m != big_m;
+            const float rl = row_l[row];
+            const size_t orow = (size_t)bt * p.Hq + g * G + row;
+            reinterpret_cast<float4*>(p.out + orow * kD)[dv] =
+                nan ? make_float4(big_m, big_m, big_m, big_m)
+                    : make_float4(acc.x / rl, acc.y / rl, acc.z / rl, acc.w / rl);
+            if (dv == 0) p.lse[orow] = row_lse[row];
+          }
         }
         if (ct == 0) p.counters[u] = 0;
       }
