@@ -304,6 +304,80 @@ int kv_mark_attention_done(kv_arena* arena, int layer);
 int kv_writeback_tail(kv_arena* arena, int layer, const kv_tail_req* reqs,
                       int n_reqs);
 
+/* ------------------------------------------------------------------------ */
+/* Leases  ([SWS-lease], [KVE-lease], "GPU memory management" / "Staging as   */
+/* a lease")                                                                */
+/* ------------------------------------------------------------------------ */
+/* Every staged layer is a transaction.  A lease is begun (the layer's pages
+ * are copied into a slot), given its attention event after the attention
+ * kernels, optionally given its tail write-back, sealed with exactly those two
+ * events, and retired: the host waits for its copy, attention and write-back
+ * events, receives a receipt, and the lease's copy tickets are released.
+ * Rules enforced (PA_ERR_ORDER otherwise, nothing submitted):
+ *   - a lease may begin only when the previously begun lease is sealed or
+ *     retired;
+ *   - a slot whose previous lease is sealed but not retired is refilled only
+ *     after that lease's attention and write-back events (device-side waits,
+ *     listed as the new lease's prior readers);
+ *   - seal must present the attention token and the write-back token (0 if
+ *     none was issued) returned for this lease: a substituted event is an
+ *     error;
+ *   - retire requires a sealed lease;
+ *   - the host pages of an owner cannot be recycled (their generation
+ *     advanced) while a live lease holds a copy ticket on them.
+ * The stage generation of each lease is strictly increasing.  An arena is
+ * driven either by these calls or by the stage calls above, not both. */
+
+typedef struct {
+    uint64_t       lease_id;    /* the lease's stage generation                 */
+    int32_t        slot;
+    int32_t        pad_;
+    const int32_t* page_table;  /* device [max_requests][max_pages] of the slot */
+} kv_lease;
+
+typedef struct {
+    uint64_t lease_id;
+    int32_t  layer;
+    int32_t  n_requests;
+    int64_t  step;
+    uint64_t staged_bytes;        /* bytes the lease copied host->device        */
+    uint64_t written_back_bytes;  /* bytes its tail write-back copied back      */
+    int32_t  tickets_released;    /* copy tickets (host owners) released        */
+    int32_t  pad_;
+} kv_receipt;
+
+/* Begin a lease for `layer` at decode `step`: validates and stages `reqs`
+ * like kv_stage_layer (each request's owner identifies the host pages it
+ * copies from; a copy ticket records that owner's current generation). */
+int kv_lease_begin(kv_arena* arena, int layer, int64_t step, const kv_stage_req* reqs,
+                   int n_reqs, kv_lease* out);
+
+/* Record the lease's attention (consumer) event on the compute stream, after
+ * the last kernel that reads its slot; returns the event's token. */
+int kv_lease_attention_done(kv_arena* arena, uint64_t lease_id, uint64_t* token);
+
+/* Tail write-back as kv_writeback_tail (owner-checked, after the attention
+ * event, on the D2H stream); returns the write-back event's token. */
+int kv_lease_writeback(kv_arena* arena, uint64_t lease_id, const kv_tail_req* reqs,
+                       int n_reqs, uint64_t* token);
+
+/* Seal with the lease's own attention token and current write-back token. */
+int kv_lease_seal(kv_arena* arena, uint64_t lease_id, uint64_t attention_token,
+                  uint64_t writeback_token);
+
+/* Host waits on the lease's copy, attention and write-back events, then the
+ * receipt; a failing wait quarantines the arena and keeps the lease. */
+int kv_lease_retire(kv_arena* arena, uint64_t lease_id, kv_receipt* receipt);
+
+/* Current generation of an owner's host pages and the live copy tickets on it. */
+int kv_host_generation(kv_arena* arena, uint64_t owner, uint64_t* generation,
+                       int64_t* live_tickets);
+
+/* Advance an owner's host-page generation (its pages may be reused for other
+ * data); refused while any live lease holds a copy ticket on them, and while
+ * the arena is quarantined. */
+int kv_host_recycle(kv_arena* arena, uint64_t owner, uint64_t* new_generation);
+
 /* Counters of the arena. */
 int kv_arena_get_stats(const kv_arena* arena, kv_arena_stats* out);
 

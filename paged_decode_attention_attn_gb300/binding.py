@@ -38,6 +38,8 @@ EXPORTED = [
     "kv_arena_create", "kv_arena_destroy", "kv_arena_drain", "kv_stage_layer",
     "kv_mark_attention_done", "kv_writeback_tail", "kv_arena_get_stats",
     "kv_arena_fail_after", "kv_arena_call_log",
+    "kv_lease_begin", "kv_lease_attention_done", "kv_lease_writeback", "kv_lease_seal",
+    "kv_lease_retire", "kv_host_generation", "kv_host_recycle",
 ]
 
 
@@ -106,6 +108,28 @@ class KvArenaStats(ctypes.Structure):
     ]
 
 
+class KvLease(ctypes.Structure):
+    _fields_ = [
+        ("lease_id", ctypes.c_uint64),
+        ("slot", ctypes.c_int32),
+        ("pad_", ctypes.c_int32),
+        ("page_table", ctypes.c_void_p),
+    ]
+
+
+class KvReceipt(ctypes.Structure):
+    _fields_ = [
+        ("lease_id", ctypes.c_uint64),
+        ("layer", ctypes.c_int32),
+        ("n_requests", ctypes.c_int32),
+        ("step", ctypes.c_int64),
+        ("staged_bytes", ctypes.c_uint64),
+        ("written_back_bytes", ctypes.c_uint64),
+        ("tickets_released", ctypes.c_int32),
+        ("pad_", ctypes.c_int32),
+    ]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -148,6 +172,22 @@ def _load():
     lib.kv_arena_fail_after.argtypes = [vp, i64]
     lib.kv_arena_call_log.restype = sz
     lib.kv_arena_call_log.argtypes = [vp, ctypes.c_char_p, sz]
+    u64p = ctypes.POINTER(ctypes.c_uint64)
+    lib.kv_lease_begin.restype = i32
+    lib.kv_lease_begin.argtypes = [vp, i32, i64, ctypes.POINTER(KvStageReq), i32,
+                                   ctypes.POINTER(KvLease)]
+    lib.kv_lease_attention_done.restype = i32
+    lib.kv_lease_attention_done.argtypes = [vp, ctypes.c_uint64, u64p]
+    lib.kv_lease_writeback.restype = i32
+    lib.kv_lease_writeback.argtypes = [vp, ctypes.c_uint64, ctypes.POINTER(KvTailReq), i32, u64p]
+    lib.kv_lease_seal.restype = i32
+    lib.kv_lease_seal.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
+    lib.kv_lease_retire.restype = i32
+    lib.kv_lease_retire.argtypes = [vp, ctypes.c_uint64, ctypes.POINTER(KvReceipt)]
+    lib.kv_host_generation.restype = i32
+    lib.kv_host_generation.argtypes = [vp, ctypes.c_uint64, u64p, ctypes.POINTER(ctypes.c_int64)]
+    lib.kv_host_recycle.restype = i32
+    lib.kv_host_recycle.argtypes = [vp, ctypes.c_uint64, u64p]
     return lib
 
 
@@ -344,6 +384,74 @@ class Arena:
             arr[i].host_row = host_row
             arr[i].owner = owner
         _check(lib.kv_writeback_tail(self.handle, layer, arr, len(tails)))
+
+    @staticmethod
+    def _stage_reqs(requests):
+        reqs = (KvStageReq * max(1, len(requests)))()
+        keep = []
+        for i, (request, owner, runs) in enumerate(requests):
+            arr = (KvPageRun * max(1, len(runs)))()
+            for k, r in enumerate(runs):
+                arr[k].logical_page = r["logical_page"]
+                arr[k].n_pages = r["n_pages"]
+                arr[k].n_rows = r.get("n_rows", 0)
+                arr[k].host_rows = r.get("host_rows")
+                arr[k].resident_page = r.get("resident_page", 0)
+            keep.append(arr)
+            reqs[i].request = request
+            reqs[i].n_runs = len(runs)
+            reqs[i].runs = ctypes.cast(arr, ctypes.POINTER(KvPageRun))
+            reqs[i].owner = owner
+        return reqs, keep
+
+    @staticmethod
+    def _tail_reqs(tails):
+        arr = (KvTailReq * max(1, len(tails)))()
+        for i, (request, position, host_row, owner) in enumerate(tails):
+            arr[i].request = request
+            arr[i].position = position
+            arr[i].host_row = host_row
+            arr[i].owner = owner
+        return arr
+
+    # ---- leases ----
+    def lease_begin(self, layer: int, step: int, requests) -> KvLease:
+        reqs, keep = self._stage_reqs(requests)
+        out = KvLease()
+        _check(lib.kv_lease_begin(self.handle, layer, step, reqs, len(requests),
+                                  ctypes.byref(out)))
+        del keep
+        return out
+
+    def lease_attention_done(self, lease_id: int) -> int:
+        tok = ctypes.c_uint64()
+        _check(lib.kv_lease_attention_done(self.handle, lease_id, ctypes.byref(tok)))
+        return tok.value
+
+    def lease_writeback(self, lease_id: int, tails) -> int:
+        tok = ctypes.c_uint64()
+        _check(lib.kv_lease_writeback(self.handle, lease_id, self._tail_reqs(tails), len(tails),
+                                      ctypes.byref(tok)))
+        return tok.value
+
+    def lease_seal(self, lease_id: int, attention_token: int, writeback_token: int = 0):
+        _check(lib.kv_lease_seal(self.handle, lease_id, attention_token, writeback_token))
+
+    def lease_retire(self, lease_id: int) -> KvReceipt:
+        r = KvReceipt()
+        _check(lib.kv_lease_retire(self.handle, lease_id, ctypes.byref(r)))
+        return r
+
+    def host_generation(self, owner: int):
+        g = ctypes.c_uint64()
+        n = ctypes.c_int64()
+        _check(lib.kv_host_generation(self.handle, owner, ctypes.byref(g), ctypes.byref(n)))
+        return g.value, n.value
+
+    def host_recycle(self, owner: int) -> int:
+        g = ctypes.c_uint64()
+        _check(lib.kv_host_recycle(self.handle, owner, ctypes.byref(g)))
+        return g.value
 
     def drain(self):
         _check(lib.kv_arena_drain(self.handle))

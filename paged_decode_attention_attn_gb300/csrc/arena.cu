@@ -16,6 +16,18 @@
 //     made for;
 //   * any failure quarantines the arena; only a drain that establishes
 //     completion releases it; destroy never waits, submits or drains.
+//
+// Two ways to drive an arena (one per arena):
+//   * the stage calls (kv_stage_layer, kv_mark_attention_done,
+//     kv_writeback_tail): a slot's next stage waits on the device for the
+//     previous stage's attention and write-back events;
+//   * leases ("Leases instead of buffers"; "Staging layers under a lease";
+//     "GPU memory management", section "Staging as a lease"): every staged
+//     layer is a transaction with a strictly increasing stage generation that
+//     is begun, given its attention event and tail write-back, sealed with
+//     exactly those events, and retired with host waits that produce a receipt.
+//     Copy tickets pin the generation of the host pages a lease copies from, so
+//     those pages cannot be recycled while a copy may still read them.
 #include <cuda_runtime.h>
 
 #include <cinttypes>
@@ -71,8 +83,39 @@ struct Slot {
   int layer = -1;
   uint64_t generation = 0;
   bool written_back = false;
+  bool retired = false;          // lease API: host confirmed completion of the last use
+  uint64_t lease_id = 0;         // lease API: lease that last used the slot
   std::vector<ReqRecord> reqs;
 };
+
+enum LeaseState { kBegun = 0, kLeaseAttended = 1, kSealed = 2 };
+
+struct Ticket {
+  uint64_t owner;
+  uint64_t host_generation;
+  uint64_t bytes;
+};
+
+struct Lease {
+  uint64_t id = 0;               // the stage generation
+  int layer = 0;
+  int64_t step = 0;
+  int slot = 0;
+  LeaseState state = kBegun;
+  uint64_t attention_token = 0;
+  uint64_t writeback_token = 0;  // 0 until a write-back is issued
+  uint64_t staged_bytes = 0;
+  uint64_t written_back_bytes = 0;
+  int32_t n_requests = 0;
+  std::vector<Ticket> tickets;
+};
+
+struct HostOwner {
+  uint64_t generation = 1;
+  int64_t live_tickets = 0;
+};
+
+enum Mode { kModeUnset = 0, kModeStage = 1, kModeLease = 2 };
 
 }  // namespace arena
 }  // namespace pa
@@ -92,6 +135,11 @@ struct kv_arena {
   uint64_t slot_reuses = 0;
   int64_t page_bytes = 0;
   int64_t arena_pages = 0;
+  pa::arena::Mode mode = pa::arena::kModeUnset;
+  std::map<uint64_t, pa::arena::Lease> leases;      // begun, not yet retired
+  std::map<uint64_t, pa::arena::HostOwner> owners;  // host page generations
+  uint64_t last_lease = 0;                          // most recently begun lease
+  uint64_t event_tokens = 0;
 };
 
 namespace pa {
@@ -154,6 +202,17 @@ int op_record(kv_arena* a, cudaStream_t s, const char* ev_kind, int slot, cudaEv
   return e == cudaSuccess ? PA_OK : quarantine(a, "cudaEventRecord", e);
 }
 
+// Host wait on an event (lease retirement); a failure quarantines.
+int op_host_wait(kv_arena* a, const char* ev_kind, int slot, cudaEvent_t ev) {
+  if (injected_failure(a)) return quarantine(a, "cudaEventSynchronize", cudaSuccess);
+  if (a->record_only) {
+    logf_(a, "host wait %s[%d]", ev_kind, slot);
+    return PA_OK;
+  }
+  const cudaError_t e = cudaEventSynchronize(ev);
+  return e == cudaSuccess ? PA_OK : quarantine(a, "cudaEventSynchronize", e);
+}
+
 int op_copy(kv_arena* a, cudaStream_t s, void* dst, const void* src, size_t bytes,
             cudaMemcpyKind kind, long long dev_page, long long row) {
   if (injected_failure(a)) return quarantine(a, "cudaMemcpyAsync", cudaSuccess);
@@ -186,6 +245,178 @@ int op_table(kv_arena* a, cudaStream_t s, int slot, const TableParams& p) {
   fill_page_table_kernel<<<blocks, 256, 0, s>>>(p);
   const cudaError_t e = cudaGetLastError();
   return e == cudaSuccess ? PA_OK : quarantine(a, "page-table kernel launch", e);
+}
+
+// Checks a stage request list against the arena; submits nothing.
+int validate_stage(kv_arena* a, const kv_stage_req* reqs, int n_reqs) {
+  const kv_arena_desc& d = a->d;
+  PA_REQUIRE(n_reqs >= 0 && (n_reqs == 0 || reqs), "bad request list");
+  std::vector<char> seen(d.max_requests, 0);
+  int64_t staged_pages = 0;
+  for (int i = 0; i < n_reqs; ++i) {
+    const kv_stage_req& r = reqs[i];
+    PA_REQUIRE(r.request >= 0 && r.request < d.max_requests, "request %d outside [0, %d)",
+               r.request, d.max_requests);
+    PA_REQUIRE(!seen[r.request], "request %d staged twice", r.request);
+    seen[r.request] = 1;
+    PA_REQUIRE(r.n_runs >= 0 && (r.n_runs == 0 || r.runs), "request %d: bad run list",
+               r.request);
+    for (int k = 0; k < r.n_runs; ++k) {
+      const kv_page_run& run = r.runs[k];
+      PA_REQUIRE(run.logical_page >= 0 && run.n_pages >= 1 &&
+                     (int64_t)run.logical_page + run.n_pages <= d.max_pages,
+                 "request %d run %d: pages [%d, +%d) outside the table", r.request, k,
+                 run.logical_page, run.n_pages);
+      if (run.host_rows) {
+        PA_REQUIRE(run.n_rows >= 0 && run.n_rows <= (int64_t)run.n_pages * d.page_tokens,
+                   "request %d run %d: %" PRId64 " rows do not fit %d pages", r.request, k,
+                   run.n_rows, run.n_pages);
+        if (!a->record_only) {
+          cudaPointerAttributes attr;
+          const cudaError_t e = cudaPointerGetAttributes(&attr, run.host_rows);
+          PA_REQUIRE(e == cudaSuccess && attr.type == cudaMemoryTypeHost,
+                     "request %d run %d: host rows must be pinned host memory", r.request, k);
+        }
+        staged_pages += run.n_pages;
+      } else {
+        PA_REQUIRE(run.resident_page >= 0 && run.resident_page + run.n_pages <= a->arena_pages,
+                   "request %d run %d: resident pages outside the arena", r.request, k);
+      }
+    }
+  }
+  PA_REQUIRE(staged_pages <= d.slot_pages, "stage needs %" PRId64 " pages, a slot holds %" PRId64,
+             staged_pages, d.slot_pages);
+  return PA_OK;
+}
+
+// Enqueues a validated stage into `slot`: optional waits on the slot's
+// previous readers, one H2D copy per staged run, the page-table fill, the copy
+// event and the compute stream's wait on it.  Returns the run records and the
+// bytes copied per request.
+int submit_stage(kv_arena* a, int slot, bool wait_prior_readers, const kv_stage_req* reqs,
+                 int n_reqs, std::vector<ReqRecord>* records, std::vector<uint64_t>* bytes) {
+  const kv_arena_desc& d = a->d;
+  Slot& S = a->slots[slot];
+  const cudaStream_t h2d = d.h2d_stream;
+  int rc;
+  if (wait_prior_readers) {
+    ++a->slot_reuses;
+    if ((rc = op_wait(a, h2d, "attn", slot, a->ev_attn[slot])) != PA_OK) return rc;
+    if (S.written_back && (rc = op_wait(a, h2d, "wb", slot, a->ev_wb[slot])) != PA_OK) return rc;
+  }
+  uint8_t* base = static_cast<uint8_t*>(d.device_base);
+  const int64_t slot_page0 = d.slot_first_page + (int64_t)slot * d.slot_pages;
+  records->clear();
+  records->reserve(n_reqs);
+  bytes->assign(n_reqs, 0);
+  std::vector<TableRun> table_runs;
+  int64_t cursor = 0;
+  for (int i = 0; i < n_reqs; ++i) {
+    const kv_stage_req& r = reqs[i];
+    ReqRecord rec;
+    rec.request = r.request;
+    rec.owner = r.owner;
+    for (int k = 0; k < r.n_runs; ++k) {
+      const kv_page_run& run = r.runs[k];
+      int64_t first;
+      if (run.host_rows) {
+        first = slot_page0 + cursor;
+        cursor += run.n_pages;
+        const size_t nb = (size_t)run.n_rows * d.row_bytes;
+        if (nb > 0) {
+          if ((rc = op_copy(a, h2d, base + first * a->page_bytes, run.host_rows, nb,
+                            cudaMemcpyHostToDevice, first, 0)) != PA_OK)
+            return rc;
+          a->staged_bytes += nb;
+          (*bytes)[i] += nb;
+        }
+      } else {
+        first = run.resident_page;
+      }
+      rec.runs.push_back(run);
+      rec.first_page.push_back(first);
+      table_runs.push_back(TableRun{r.request, run.logical_page, run.n_pages, 0, first});
+    }
+    records->push_back(std::move(rec));
+  }
+  int32_t* table = d.page_tables + (size_t)slot * d.max_requests * d.max_pages;
+  for (size_t r0 = 0; r0 < table_runs.size(); r0 += kMaxRunsPerLaunch) {
+    TableParams tp{};
+    tp.table = table;
+    tp.max_pages = d.max_pages;
+    tp.n_runs = static_cast<int>(std::min<size_t>(kMaxRunsPerLaunch, table_runs.size() - r0));
+    std::memcpy(tp.runs, table_runs.data() + r0, tp.n_runs * sizeof(TableRun));
+    if ((rc = op_table(a, h2d, slot, tp)) != PA_OK) return rc;
+  }
+  if ((rc = op_record(a, h2d, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
+  if ((rc = op_wait(a, d.compute_stream, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
+  return PA_OK;
+}
+
+// Resolves each tail row's device address in `slot` and checks its owner;
+// submits nothing.
+int resolve_tails(kv_arena* a, int slot, int layer, const kv_tail_req* reqs, int n_reqs,
+                  std::vector<uint8_t*>* src) {
+  const kv_arena_desc& d = a->d;
+  const Slot& S = a->slots[slot];
+  PA_REQUIRE(n_reqs >= 0 && (n_reqs == 0 || reqs), "bad request list");
+  src->assign(n_reqs, nullptr);
+  for (int i = 0; i < n_reqs; ++i) {
+    const kv_tail_req& t = reqs[i];
+    PA_REQUIRE(t.host_row != nullptr, "tail %d: null host row", i);
+    const ReqRecord* rec = nullptr;
+    for (const auto& r : S.reqs)
+      if (r.request == t.request) rec = &r;
+    PA_REQUIRE(rec != nullptr, "tail %d: request %d was not staged for layer %d", i, t.request,
+               layer);
+    if (rec->owner != t.owner)
+      return fail(PA_ERR_OWNER,
+                  "tail %d: owner %" PRIu64 " differs from the owner %" PRIu64
+                  " request %d was staged with",
+                  i, t.owner, rec->owner, t.request);
+    PA_REQUIRE(t.position >= 0, "tail %d: negative position", i);
+    const int64_t lp = t.position / d.page_tokens;
+    int64_t page = -1;
+    for (size_t k = 0; k < rec->runs.size(); ++k) {
+      const kv_page_run& run = rec->runs[k];
+      if (lp >= run.logical_page && lp < (int64_t)run.logical_page + run.n_pages)
+        page = rec->first_page[k] + (lp - run.logical_page);
+    }
+    PA_REQUIRE(page >= 0, "tail %d: position %" PRId64 " is not in a staged or resident run", i,
+               t.position);
+    (*src)[i] = static_cast<uint8_t*>(d.device_base) +
+                (page * d.page_tokens + t.position % d.page_tokens) * (int64_t)d.row_bytes;
+  }
+  return PA_OK;
+}
+
+// Enqueues the tail write-backs of `slot` after its attention event and
+// records the write-back event.
+int submit_tails(kv_arena* a, int slot, const kv_tail_req* reqs, int n_reqs,
+                 const std::vector<uint8_t*>& src, uint64_t* bytes) {
+  const kv_arena_desc& d = a->d;
+  int rc;
+  if ((rc = op_wait(a, d.d2h_stream, "attn", slot, a->ev_attn[slot])) != PA_OK) return rc;
+  for (int i = 0; i < n_reqs; ++i) {
+    const int64_t off = src[i] - static_cast<uint8_t*>(d.device_base);
+    if ((rc = op_copy(a, d.d2h_stream, reqs[i].host_row, src[i], d.row_bytes,
+                      cudaMemcpyDeviceToHost, off / a->page_bytes,
+                      (off % a->page_bytes) / d.row_bytes)) != PA_OK)
+      return rc;
+    a->written_back_bytes += d.row_bytes;
+    *bytes += d.row_bytes;
+  }
+  if ((rc = op_record(a, d.d2h_stream, "wb", slot, a->ev_wb[slot])) != PA_OK) return rc;
+  a->slots[slot].written_back = true;
+  return PA_OK;
+}
+
+int use_mode(kv_arena* a, Mode m) {
+  if (a->mode == kModeUnset) a->mode = m;
+  if (a->mode != m)
+    return fail(PA_ERR_ORDER, "this arena is driven by %s calls; do not mix the two",
+                a->mode == kModeStage ? "stage" : "lease");
+  return PA_OK;
 }
 
 }  // namespace
@@ -265,16 +496,28 @@ extern "C" int kv_arena_drain(kv_arena* a) {
       if (e != cudaSuccess) return quarantine(a, "cudaStreamSynchronize", e);
     }
   }
-  // Completion is established: every slot is free again.
+  // Completion is established: every slot is free again; leases that were
+  // in flight are dropped (their copies are known to be finished) and their
+  // tickets released.
   for (auto& s : a->slots) {
     s.state = kFree;
     s.written_back = false;
+    s.retired = false;
+    s.lease_id = 0;
     s.reqs.clear();
   }
+  for (auto& kv : a->leases)
+    for (const Ticket& t : kv.second.tickets) a->owners[t.owner].live_tickets -= 1;
+  a->leases.clear();
+  a->last_lease = 0;
   a->layer_slot.clear();
   a->quarantined = false;
   return PA_OK;
 }
+
+// ---------------------------------------------------------------------------
+// Stage calls.
+// ---------------------------------------------------------------------------
 
 extern "C" int kv_stage_layer(kv_arena* a, int layer, const kv_stage_req* reqs, int n_reqs,
                               int* slot_out, const int32_t** page_table_out) {
@@ -282,7 +525,8 @@ extern "C" int kv_stage_layer(kv_arena* a, int layer, const kv_stage_req* reqs, 
   PA_REQUIRE(a, "null arena");
   if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
   PA_REQUIRE(layer >= 0, "layer must be >= 0");
-  PA_REQUIRE(n_reqs >= 0 && (n_reqs == 0 || reqs), "bad request list");
+  int rc = use_mode(a, kModeStage);
+  if (rc != PA_OK) return rc;
   const kv_arena_desc& d = a->d;
   const int slot = static_cast<int>(a->generation % (uint64_t)d.n_slots);
   Slot& S = a->slots[slot];
@@ -290,100 +534,11 @@ extern "C" int kv_stage_layer(kv_arena* a, int layer, const kv_stage_req* reqs, 
     return fail(PA_ERR_ORDER,
                 "slot %d still holds layer %d, which was never marked attention-done", slot,
                 S.layer);
-
-  // ---- validate everything before submitting anything ----
-  std::vector<char> seen(d.max_requests, 0);
-  int64_t staged_pages = 0;
-  int n_table_runs = 0;
-  for (int i = 0; i < n_reqs; ++i) {
-    const kv_stage_req& r = reqs[i];
-    PA_REQUIRE(r.request >= 0 && r.request < d.max_requests, "request %d outside [0, %d)",
-               r.request, d.max_requests);
-    PA_REQUIRE(!seen[r.request], "request %d staged twice", r.request);
-    seen[r.request] = 1;
-    PA_REQUIRE(r.n_runs >= 0 && (r.n_runs == 0 || r.runs), "request %d: bad run list",
-               r.request);
-    for (int k = 0; k < r.n_runs; ++k) {
-      const kv_page_run& run = r.runs[k];
-      PA_REQUIRE(run.logical_page >= 0 && run.n_pages >= 1 &&
-                     (int64_t)run.logical_page + run.n_pages <= d.max_pages,
-                 "request %d run %d: pages [%d, +%d) outside the table", r.request, k,
-                 run.logical_page, run.n_pages);
-      if (run.host_rows) {
-        PA_REQUIRE(run.n_rows >= 0 && run.n_rows <= (int64_t)run.n_pages * d.page_tokens,
-                   "request %d run %d: %" PRId64 " rows do not fit %d pages", r.request, k,
-                   run.n_rows, run.n_pages);
-        if (!a->record_only) {
-          cudaPointerAttributes attr;
-          const cudaError_t e = cudaPointerGetAttributes(&attr, run.host_rows);
-          PA_REQUIRE(e == cudaSuccess && attr.type == cudaMemoryTypeHost,
-                     "request %d run %d: host rows must be pinned host memory", r.request, k);
-        }
-        staged_pages += run.n_pages;
-      } else {
-        PA_REQUIRE(run.resident_page >= 0 && run.resident_page + run.n_pages <= a->arena_pages,
-                   "request %d run %d: resident pages outside the arena", r.request, k);
-      }
-      ++n_table_runs;
-    }
-  }
-  PA_REQUIRE(staged_pages <= d.slot_pages, "stage needs %" PRId64 " pages, a slot holds %" PRId64,
-             staged_pages, d.slot_pages);
-
-  // ---- submit ----
-  const cudaStream_t h2d = d.h2d_stream;
-  int rc;
-  if (S.state != kFree) {
-    ++a->slot_reuses;
-    if ((rc = op_wait(a, h2d, "attn", slot, a->ev_attn[slot])) != PA_OK) return rc;
-    if (S.written_back && (rc = op_wait(a, h2d, "wb", slot, a->ev_wb[slot])) != PA_OK) return rc;
-  }
-  uint8_t* base = static_cast<uint8_t*>(d.device_base);
-  const int64_t slot_page0 = d.slot_first_page + (int64_t)slot * d.slot_pages;
+  if ((rc = validate_stage(a, reqs, n_reqs)) != PA_OK) return rc;
   std::vector<ReqRecord> records;
-  records.reserve(n_reqs);
-  std::vector<TableRun> table_runs;
-  table_runs.reserve(n_table_runs);
-  int64_t cursor = 0;
-  for (int i = 0; i < n_reqs; ++i) {
-    const kv_stage_req& r = reqs[i];
-    ReqRecord rec;
-    rec.request = r.request;
-    rec.owner = r.owner;
-    for (int k = 0; k < r.n_runs; ++k) {
-      const kv_page_run& run = r.runs[k];
-      int64_t first;
-      if (run.host_rows) {
-        first = slot_page0 + cursor;
-        cursor += run.n_pages;
-        const size_t bytes = (size_t)run.n_rows * d.row_bytes;
-        if (bytes > 0) {
-          if ((rc = op_copy(a, h2d, base + first * a->page_bytes, run.host_rows, bytes,
-                            cudaMemcpyHostToDevice, first, 0)) != PA_OK)
-            return rc;
-          a->staged_bytes += bytes;
-        }
-      } else {
-        first = run.resident_page;
-      }
-      rec.runs.push_back(run);
-      rec.first_page.push_back(first);
-      table_runs.push_back(TableRun{r.request, run.logical_page, run.n_pages, 0, first});
-    }
-    records.push_back(std::move(rec));
-  }
-  int32_t* table = d.page_tables + (size_t)slot * d.max_requests * d.max_pages;
-  for (size_t r0 = 0; r0 < table_runs.size(); r0 += kMaxRunsPerLaunch) {
-    TableParams tp{};
-    tp.table = table;
-    tp.max_pages = d.max_pages;
-    tp.n_runs = static_cast<int>(std::min<size_t>(kMaxRunsPerLaunch, table_runs.size() - r0));
-    std::memcpy(tp.runs, table_runs.data() + r0, tp.n_runs * sizeof(TableRun));
-    if ((rc = op_table(a, h2d, slot, tp)) != PA_OK) return rc;
-  }
-  if ((rc = op_record(a, h2d, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
-  if ((rc = op_wait(a, d.compute_stream, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
-
+  std::vector<uint64_t> bytes;
+  if ((rc = submit_stage(a, slot, S.state != kFree, reqs, n_reqs, &records, &bytes)) != PA_OK)
+    return rc;
   S.state = kStaged;
   S.layer = layer;
   S.generation = ++a->generation;
@@ -391,7 +546,7 @@ extern "C" int kv_stage_layer(kv_arena* a, int layer, const kv_stage_req* reqs, 
   S.reqs = std::move(records);
   a->layer_slot[layer] = slot;
   if (slot_out) *slot_out = slot;
-  if (page_table_out) *page_table_out = table;
+  if (page_table_out) *page_table_out = d.page_tables + (size_t)slot * d.max_requests * d.max_pages;
   return PA_OK;
 }
 
@@ -399,12 +554,14 @@ extern "C" int kv_mark_attention_done(kv_arena* a, int layer) {
   pa::clear_error();
   PA_REQUIRE(a, "null arena");
   if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  int rc = use_mode(a, kModeStage);
+  if (rc != PA_OK) return rc;
   const auto it = a->layer_slot.find(layer);
   if (it == a->layer_slot.end()) return fail(PA_ERR_ORDER, "layer %d has no current stage", layer);
   Slot& S = a->slots[it->second];
   if (S.layer != layer || S.state != kStaged)
     return fail(PA_ERR_ORDER, "layer %d is not awaiting attention (slot %d)", layer, it->second);
-  const int rc = op_record(a, a->d.compute_stream, "attn", it->second, a->ev_attn[it->second]);
+  rc = op_record(a, a->d.compute_stream, "attn", it->second, a->ev_attn[it->second]);
   if (rc != PA_OK) return rc;
   S.state = kAttended;
   return PA_OK;
@@ -414,7 +571,8 @@ extern "C" int kv_writeback_tail(kv_arena* a, int layer, const kv_tail_req* reqs
   pa::clear_error();
   PA_REQUIRE(a, "null arena");
   if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
-  PA_REQUIRE(n_reqs >= 0 && (n_reqs == 0 || reqs), "bad request list");
+  int rc = use_mode(a, kModeStage);
+  if (rc != PA_OK) return rc;
   const auto it = a->layer_slot.find(layer);
   if (it == a->layer_slot.end()) return fail(PA_ERR_ORDER, "layer %d has no current stage", layer);
   const int slot = it->second;
@@ -422,46 +580,193 @@ extern "C" int kv_writeback_tail(kv_arena* a, int layer, const kv_tail_req* reqs
   if (S.layer != layer || S.state != kAttended)
     return fail(PA_ERR_ORDER, "write-back of layer %d before its attention was marked done",
                 layer);
+  std::vector<uint8_t*> src;
+  if ((rc = resolve_tails(a, slot, layer, reqs, n_reqs, &src)) != PA_OK) return rc;
+  uint64_t bytes = 0;
+  return submit_tails(a, slot, reqs, n_reqs, src, &bytes);
+}
+
+// ---------------------------------------------------------------------------
+// Leases.
+// ---------------------------------------------------------------------------
+
+extern "C" int kv_lease_begin(kv_arena* a, int layer, int64_t step, const kv_stage_req* reqs,
+                              int n_reqs, kv_lease* out) {
+  pa::clear_error();
+  PA_REQUIRE(a && out, "null pointer argument");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  PA_REQUIRE(layer >= 0, "layer must be >= 0");
+  int rc = use_mode(a, kModeLease);
+  if (rc != PA_OK) return rc;
+  // A new lease may begin only once the previous one is sealed or retired.
+  if (a->last_lease != 0) {
+    const auto prev = a->leases.find(a->last_lease);
+    if (prev != a->leases.end() && prev->second.state != kSealed)
+      return fail(PA_ERR_ORDER, "lease %" PRIu64 " (layer %d) is neither sealed nor retired",
+                  prev->second.id, prev->second.layer);
+  }
   const kv_arena_desc& d = a->d;
-  std::vector<uint8_t*> src(n_reqs);
+  const int slot = static_cast<int>(a->generation % (uint64_t)d.n_slots);
+  Slot& S = a->slots[slot];
+  if ((rc = validate_stage(a, reqs, n_reqs)) != PA_OK) return rc;
+  // The previous user of the slot is sealed (checked above or earlier).  If
+  // it is not retired, its attention and write-back are prior readers of this
+  // lease: the copies wait for them on the device.
+  const bool wait_prior = S.state != kFree && !S.retired;
+  std::vector<ReqRecord> records;
+  std::vector<uint64_t> bytes;
+  if ((rc = submit_stage(a, slot, wait_prior, reqs, n_reqs, &records, &bytes)) != PA_OK) return rc;
+  Lease L;
+  L.id = ++a->generation;
+  L.layer = layer;
+  L.step = step;
+  L.slot = slot;
+  L.n_requests = n_reqs;
   for (int i = 0; i < n_reqs; ++i) {
-    const kv_tail_req& t = reqs[i];
-    PA_REQUIRE(t.host_row != nullptr, "tail %d: null host row", i);
-    const ReqRecord* rec = nullptr;
-    for (const auto& r : S.reqs)
-      if (r.request == t.request) rec = &r;
-    PA_REQUIRE(rec != nullptr, "tail %d: request %d was not staged for layer %d", i, t.request,
-               layer);
-    if (rec->owner != t.owner)
-      return fail(PA_ERR_OWNER,
-                  "tail %d: owner %" PRIu64 " differs from the owner %" PRIu64
-                  " request %d was staged with",
-                  i, t.owner, rec->owner, t.request);
-    PA_REQUIRE(t.position >= 0, "tail %d: negative position", i);
-    const int64_t lp = t.position / d.page_tokens;
-    int64_t page = -1;
-    for (size_t k = 0; k < rec->runs.size(); ++k) {
-      const kv_page_run& run = rec->runs[k];
-      if (lp >= run.logical_page && lp < (int64_t)run.logical_page + run.n_pages)
-        page = rec->first_page[k] + (lp - run.logical_page);
+    L.staged_bytes += bytes[i];
+    bool staged = false;
+    for (int k = 0; k < reqs[i].n_runs; ++k) staged |= reqs[i].runs[k].host_rows != nullptr;
+    if (staged) {
+      HostOwner& o = a->owners[reqs[i].owner];
+      o.live_tickets += 1;
+      L.tickets.push_back(Ticket{reqs[i].owner, o.generation, bytes[i]});
     }
-    PA_REQUIRE(page >= 0, "tail %d: position %" PRId64 " is not in a staged or resident run", i,
-               t.position);
-    src[i] = static_cast<uint8_t*>(d.device_base) +
-             (page * d.page_tokens + t.position % d.page_tokens) * (int64_t)d.row_bytes;
   }
+  S.state = kStaged;
+  S.layer = layer;
+  S.generation = L.id;
+  S.written_back = false;
+  S.retired = false;
+  S.lease_id = L.id;
+  S.reqs = std::move(records);
+  a->leases[L.id] = L;
+  a->last_lease = L.id;
+  out->lease_id = L.id;
+  out->slot = slot;
+  out->page_table = d.page_tables + (size_t)slot * d.max_requests * d.max_pages;
+  return PA_OK;
+}
+
+namespace {
+pa::arena::Lease* find_lease(kv_arena* a, uint64_t id) {
+  const auto it = a->leases.find(id);
+  return it == a->leases.end() ? nullptr : &it->second;
+}
+}  // namespace
+
+extern "C" int kv_lease_attention_done(kv_arena* a, uint64_t lease_id, uint64_t* token) {
+  pa::clear_error();
+  PA_REQUIRE(a && token, "null pointer argument");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  Lease* L = find_lease(a, lease_id);
+  if (!L) return fail(PA_ERR_ORDER, "lease %" PRIu64 " is not live", lease_id);
+  if (L->state != kBegun)
+    return fail(PA_ERR_ORDER, "lease %" PRIu64 " already has its attention event", lease_id);
+  const int rc = op_record(a, a->d.compute_stream, "attn", L->slot, a->ev_attn[L->slot]);
+  if (rc != PA_OK) return rc;
+  L->state = kLeaseAttended;
+  L->attention_token = ++a->event_tokens;
+  a->slots[L->slot].state = kAttended;
+  *token = L->attention_token;
+  return PA_OK;
+}
+
+extern "C" int kv_lease_writeback(kv_arena* a, uint64_t lease_id, const kv_tail_req* reqs,
+                                  int n_reqs, uint64_t* token) {
+  pa::clear_error();
+  PA_REQUIRE(a && token, "null pointer argument");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  Lease* L = find_lease(a, lease_id);
+  if (!L) return fail(PA_ERR_ORDER, "lease %" PRIu64 " is not live", lease_id);
+  if (L->state != kLeaseAttended)
+    return fail(PA_ERR_ORDER, "lease %" PRIu64 ": write-back needs its attention event first%s",
+                lease_id, L->state == kSealed ? " (and the lease is already sealed)" : "");
+  std::vector<uint8_t*> src;
+  int rc = resolve_tails(a, L->slot, L->layer, reqs, n_reqs, &src);
+  if (rc != PA_OK) return rc;
+  if ((rc = submit_tails(a, L->slot, reqs, n_reqs, src, &L->written_back_bytes)) != PA_OK)
+    return rc;
+  L->writeback_token = ++a->event_tokens;
+  *token = L->writeback_token;
+  return PA_OK;
+}
+
+extern "C" int kv_lease_seal(kv_arena* a, uint64_t lease_id, uint64_t attention_token,
+                             uint64_t writeback_token) {
+  pa::clear_error();
+  PA_REQUIRE(a, "null arena");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  Lease* L = find_lease(a, lease_id);
+  if (!L) return fail(PA_ERR_ORDER, "lease %" PRIu64 " is not live", lease_id);
+  if (L->state == kBegun)
+    return fail(PA_ERR_ORDER, "lease %" PRIu64 " has no attention event to seal with", lease_id);
+  if (L->state == kSealed) return fail(PA_ERR_ORDER, "lease %" PRIu64 " is already sealed", lease_id);
+  if (attention_token != L->attention_token)
+    return fail(PA_ERR_ORDER,
+                "lease %" PRIu64 ": attention event %" PRIu64 " is not the one recorded (%" PRIu64
+                "); a substituted event cannot seal",
+                lease_id, attention_token, L->attention_token);
+  if (writeback_token != L->writeback_token)
+    return fail(PA_ERR_ORDER,
+                "lease %" PRIu64 ": tail write-back %" PRIu64 " is not the current one (%" PRIu64
+                ")",
+                lease_id, writeback_token, L->writeback_token);
+  L->state = kSealed;
+  return PA_OK;
+}
+
+extern "C" int kv_lease_retire(kv_arena* a, uint64_t lease_id, kv_receipt* receipt) {
+  pa::clear_error();
+  PA_REQUIRE(a && receipt, "null pointer argument");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  Lease* L = find_lease(a, lease_id);
+  if (!L) return fail(PA_ERR_ORDER, "lease %" PRIu64 " is not live", lease_id);
+  if (L->state != kSealed)
+    return fail(PA_ERR_ORDER, "lease %" PRIu64 " must be sealed before it is retired", lease_id);
+  // Waits that fail quarantine the arena and keep the lease and its tickets.
   int rc;
-  if ((rc = op_wait(a, d.d2h_stream, "attn", slot, a->ev_attn[slot])) != PA_OK) return rc;
-  for (int i = 0; i < n_reqs; ++i) {
-    const int64_t off = src[i] - static_cast<uint8_t*>(d.device_base);
-    if ((rc = op_copy(a, d.d2h_stream, reqs[i].host_row, src[i], d.row_bytes,
-                      cudaMemcpyDeviceToHost, off / a->page_bytes,
-                      (off % a->page_bytes) / d.row_bytes)) != PA_OK)
-      return rc;
-    a->written_back_bytes += d.row_bytes;
-  }
-  if ((rc = op_record(a, d.d2h_stream, "wb", slot, a->ev_wb[slot])) != PA_OK) return rc;
-  S.written_back = true;
+  const int slot = L->slot;
+  if ((rc = op_host_wait(a, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
+  if ((rc = op_host_wait(a, "attn", slot, a->ev_attn[slot])) != PA_OK) return rc;
+  if (L->writeback_token != 0 && (rc = op_host_wait(a, "wb", slot, a->ev_wb[slot])) != PA_OK)
+    return rc;
+  receipt->lease_id = L->id;
+  receipt->layer = L->layer;
+  receipt->n_requests = L->n_requests;
+  receipt->step = L->step;
+  receipt->staged_bytes = L->staged_bytes;
+  receipt->written_back_bytes = L->written_back_bytes;
+  receipt->tickets_released = static_cast<int32_t>(L->tickets.size());
+  for (const Ticket& t : L->tickets) a->owners[t.owner].live_tickets -= 1;
+  Slot& S = a->slots[slot];
+  if (S.lease_id == L->id) S.retired = true;
+  a->leases.erase(lease_id);
+  return PA_OK;
+}
+
+extern "C" int kv_host_generation(kv_arena* a, uint64_t owner, uint64_t* generation,
+                                  int64_t* live_tickets) {
+  pa::clear_error();
+  PA_REQUIRE(a && generation, "null pointer argument");
+  const HostOwner& o = a->owners[owner];
+  *generation = o.generation;
+  if (live_tickets) *live_tickets = o.live_tickets;
+  return PA_OK;
+}
+
+extern "C" int kv_host_recycle(kv_arena* a, uint64_t owner, uint64_t* new_generation) {
+  pa::clear_error();
+  PA_REQUIRE(a, "null arena");
+  if (a->quarantined)
+    return fail(PA_ERR_QUARANTINED, "arena is quarantined: completion of its copies is unknown");
+  HostOwner& o = a->owners[owner];
+  if (o.live_tickets > 0)
+    return fail(PA_ERR_ORDER,
+                "host pages of owner %" PRIu64 " are held by %" PRId64
+                " copy ticket(s); retire those leases first",
+                owner, o.live_tickets);
+  o.generation += 1;
+  if (new_generation) *new_generation = o.generation;
   return PA_OK;
 }
 

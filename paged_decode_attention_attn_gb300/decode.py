@@ -145,9 +145,12 @@ class StagedDecode:
 
     def __init__(self, w: DecodeWorkload, t: dict, host: HostHistory, n_slots: int = 2,
                  cuda_core: bool = False, compute_stream=None, h2d_stream=None,
-                 d2h_stream=None):
+                 d2h_stream=None, leases: bool = False):
         geo = w.geometry
         self.w, self.t, self.host, self.cuda_core = w, t, host, cuda_core
+        self.leases = leases
+        self.step_index = 0
+        self.receipts = []
         self.n_layers = t["pool"].shape[0]
         dev = t["pool"].device
         self.compute = compute_stream or torch.cuda.current_stream(dev)
@@ -216,6 +219,32 @@ class StagedDecode:
                                 host.row_address(i, r, int(w.lengths[r]) - 1), (i << 32) | r)
                                for r in range(w.batch)])
 
+    def _kernels(self, i: int, table):
+        t, o, geo = self.t, self.o, self.w.geometry
+        B.kv_append_rows(self.arena, table, t["positions"], t["new_rows"][i], status=self.status,
+                         stream=self.compute)
+        B.paged_decode_attn_lse(t["q"][i], self.arena, table, self.tiles, geo.scale,
+                                o.tile_out[i], o.tile_lse[i], self.workspace,
+                                stream=self.compute, cuda_core=self.cuda_core)
+        B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
+                    o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i], o.lse[i],
+                    stream=self.compute)
+
+    def _lease_step(self):
+        """One step as leases: begin, kernels, attention event, tail write-back
+        and seal per layer; every lease is retired (host waits, receipts) at
+        the end of the step."""
+        live = []
+        for i in range(self.n_layers):
+            lease = self.handle.lease_begin(i, self.step_index, self.plan[i])
+            self._kernels(i, self.page_tables[lease.slot])
+            att = self.handle.lease_attention_done(lease.lease_id)
+            wb = self.handle.lease_writeback(lease.lease_id, self.tails[i])
+            self.handle.lease_seal(lease.lease_id, att, wb)
+            live.append(lease.lease_id)
+        self.receipts = [self.handle.lease_retire(lid) for lid in live]
+        self.step_index += 1
+
     def layer(self, i: int):
         t, o, geo = self.t, self.o, self.w.geometry
         slot, _ = self.handle.stage_layer(i, self.plan[i])
@@ -232,6 +261,9 @@ class StagedDecode:
         self.handle.writeback_tail(i, self.tails[i])
 
     def step(self):
+        if self.leases:
+            self._lease_step()
+            return
         for i in range(self.n_layers):
             self.layer(i)
 

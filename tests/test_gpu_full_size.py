@@ -75,14 +75,16 @@ def test_full_size_resident_matches_oracle(D, name):
     _free()
 
 
-@pytest.mark.parametrize("name,n_slots", [("4x31744", 2), ("4x31744", 1), ("1x262144", 2),
-                                          ("ragged-window", 2)])
-def test_staged_route_is_bit_identical_to_resident(D, name, n_slots):
+@pytest.mark.parametrize("name,n_slots,leases", [("4x31744", 2, False), ("4x31744", 1, False),
+                                                 ("1x262144", 2, False),
+                                                 ("ragged-window", 2, False),
+                                                 ("4x31744", 2, True), ("ragged-window", 1, True)])
+def test_staged_route_is_bit_identical_to_resident(D, name, n_slots, leases):
     make, _ = FULL[name]
     w = make(n_layers=3)
     t = wl.materialize(w, "cuda")
     host = D.HostHistory(w, t)
-    staged = D.StagedDecode(w, t, host, n_slots=n_slots)
+    staged = D.StagedDecode(w, t, host, n_slots=n_slots, leases=leases)
     res = D.ResidentDecode(w, t)
     res.step()
     torch.cuda.synchronize()
@@ -101,6 +103,13 @@ def test_staged_route_is_bit_identical_to_resident(D, name, n_slots):
     st = staged.handle.stats()
     assert st.stage_generation == w.n_layers and st.quarantined == 0
     assert st.written_back_bytes == w.n_layers * w.batch * w.geometry.row_bytes
+    if leases:
+        assert [r.layer for r in staged.receipts] == list(range(w.n_layers))
+        assert sum(r.staged_bytes for r in staged.receipts) == st.staged_bytes
+        assert all(r.written_back_bytes == w.batch * w.geometry.row_bytes
+                   for r in staged.receipts)
+        for r in range(w.batch):
+            assert staged.handle.host_generation((0 << 32) | r)[1] == 0   # tickets released
     staged.close()
     host.close()
     del staged, res, host, t
