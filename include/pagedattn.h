@@ -69,6 +69,7 @@ extern "C" {
 #define PA_ERR_ORDER        -4  /* slot busy or call out of order */
 #define PA_ERR_OWNER        -5  /* write-back owner differs from the staged owner */
 #define PA_ERR_UNSUPPORTED  -6  /* geometry not built into this library */
+#define PA_ERR_REFUSED      -7  /* admission refused (the caller queues the request) */
 
 /* Bits OR-ed into the int32 status word at byte 0 of the decode workspace
  * (and of the optional status word of kv_append_rows) by device code. */
@@ -388,6 +389,93 @@ int kv_arena_get_stats(const kv_arena* arena, kv_arena_stats* out);
  * buf, returns the full length. */
 int kv_arena_fail_after(kv_arena* arena, int64_t n);
 size_t kv_arena_call_log(const kv_arena* arena, char* buf, size_t buf_bytes);
+
+/* ------------------------------------------------------------------------ */
+/* Admission planner  ("Staging without a stall" / "Admission that does      */
+/* arithmetic"; "GPU memory management" / "Pages held by right, borrowed or  */
+/* free", "A host pool that explains its own size")                         */
+/* ------------------------------------------------------------------------ */
+/* Host-side bookkeeping of which logical pages of each context sit in the
+ * device page pool.  A pool page holds one page_tokens-token logical page of
+ * one context for all n_layers layers.  Each step, per listed context, the
+ * planner wants the sink pages plus the newest pages up to target + burst,
+ * and fills each missing page (sink first, then newest to oldest) by:
+ *   1. reusing one of the context's own pool pages that left its window,
+ *   2. taking a free pool page,
+ *   3. reclaiming, only while the context holds fewer than its target:
+ *      borrowed (burst) pages of other contexts, then other pages above a
+ *      target, then whole idle contexts (not listed this step), each least
+ *      recently active first,
+ *   4. else the rest of the window (its older pages) stays cold.
+ * Pages taken beyond the target are borrowed.  A context that ends the step
+ * with fewer than its floor (sink pages + 1, capped by its length) is
+ * refused for the step.  Every decision is counted; pages that became
+ * resident are reported as copied in (once).  Changes happen only inside
+ * kv_planner_step. */
+
+typedef struct kv_planner kv_planner;
+
+typedef struct {
+    uint32_t pool_gib;           /* explicit whole GiB of device pool; 0 refused   */
+    int32_t  n_layers;           /* dense layers sharing the pool                  */
+    int32_t  row_bytes;          /* bytes per token per layer (4,096 here)         */
+    int32_t  page_tokens;        /* tokens per page (PA_PAGE_TOKENS)               */
+    int32_t  sink_pages;         /* attention-sink pages kept hot (1)              */
+    int32_t  max_contexts;       /* configured concurrency limit                   */
+    uint64_t host_pool_bytes;    /* pinned host pool owning the histories          */
+    int64_t  max_context_tokens; /* context length each history must hold          */
+    int32_t  shrink_mode;        /* 0: refuse a host pool that does not fit;
+                                    1: lower the concurrency to what fits          */
+    int32_t  pad_;
+} kv_planner_desc;
+
+typedef struct {
+    uint64_t steps;
+    uint64_t reused_own;             /* pages refilled from the context's own spare */
+    uint64_t took_free;              /* pages taken from the free list              */
+    uint64_t reclaimed_borrowed;     /* borrowed pages taken from other contexts    */
+    uint64_t reclaimed_above_target; /* other above-target pages taken              */
+    uint64_t reclaimed_idle_contexts;/* idle contexts emptied                       */
+    uint64_t reclaimed_idle_pages;   /* pages freed by emptying idle contexts       */
+    uint64_t shrunk_pages;           /* wanted pages left cold                      */
+    uint64_t refused;                /* context-steps refused (below the floor)     */
+    uint64_t copied_in;              /* pages that turned hot (one copy each)       */
+    int64_t  free_pages;             /* free pool pages now                         */
+} kv_planner_counters;
+
+/* Create a planner.  The concurrency is min(max_contexts, floor(host_pool_bytes
+ * / (n_layers x max_context_tokens x row_bytes))); the formula (and the pool
+ * size in pages) is written to `formula`.  Refuse mode: PA_ERR_INVALID naming
+ * the settings to change when the host pool holds fewer than max_contexts
+ * histories; shrink mode lowers the concurrency instead. */
+int kv_planner_create(const kv_planner_desc* desc, kv_planner** out, char* formula,
+                      size_t formula_bytes);
+int kv_planner_destroy(kv_planner* planner);
+int kv_planner_info(const kv_planner* planner, int64_t* pool_pages, int* concurrency,
+                    char* formula, size_t formula_bytes);
+
+/* Admit a context (PA_ERR_REFUSED at the concurrency limit: queue it). */
+int kv_planner_admit(kv_planner* planner, uint64_t ctx, int target_pages, int burst_pages);
+int kv_planner_set_target(kv_planner* planner, uint64_t ctx, int target_pages,
+                          int burst_pages);
+/* Free every pool page of a finished context. */
+int kv_planner_release(kv_planner* planner, uint64_t ctx);
+
+/* One step boundary: the contexts running this step with their lengths
+ * (tokens, including the new one).  admitted[i] (optional) = 1 if context i
+ * reached its floor, 0 if refused for this step. */
+int kv_planner_step(kv_planner* planner, const uint64_t* ctx_ids, const int64_t* lengths,
+                    int n, int32_t* admitted);
+
+/* The context's resident pages after the last step, by increasing logical
+ * page: logical[k] lives in pool page pool[k].  *n_out = count (may exceed
+ * cap; only cap entries are written). */
+int kv_planner_resident(const kv_planner* planner, uint64_t ctx, int32_t* logical,
+                        int32_t* pool, int cap, int* n_out);
+/* Logical pages that became resident at the last step (to copy in once). */
+int kv_planner_copied(const kv_planner* planner, uint64_t ctx, int32_t* logical, int cap,
+                      int* n_out);
+int kv_planner_get_counters(const kv_planner* planner, kv_planner_counters* out);
 
 #ifdef __cplusplus
 }

@@ -23,6 +23,7 @@ PA_ERR_QUARANTINED = -3
 PA_ERR_ORDER = -4
 PA_ERR_OWNER = -5
 PA_ERR_UNSUPPORTED = -6
+PA_ERR_REFUSED = -7
 PA_STATUS_BAD_PAGE = 1
 PA_STATUS_TIMEOUT = 2
 PA_STATUS_BAD_ROW = 4
@@ -40,6 +41,9 @@ EXPORTED = [
     "kv_arena_fail_after", "kv_arena_call_log",
     "kv_lease_begin", "kv_lease_attention_done", "kv_lease_writeback", "kv_lease_seal",
     "kv_lease_retire", "kv_host_generation", "kv_host_recycle",
+    "kv_planner_create", "kv_planner_destroy", "kv_planner_info", "kv_planner_admit",
+    "kv_planner_set_target", "kv_planner_release", "kv_planner_step", "kv_planner_resident",
+    "kv_planner_copied", "kv_planner_get_counters",
 ]
 
 
@@ -130,6 +134,31 @@ class KvReceipt(ctypes.Structure):
     ]
 
 
+class KvPlannerDesc(ctypes.Structure):
+    _fields_ = [
+        ("pool_gib", ctypes.c_uint32),
+        ("n_layers", ctypes.c_int32),
+        ("row_bytes", ctypes.c_int32),
+        ("page_tokens", ctypes.c_int32),
+        ("sink_pages", ctypes.c_int32),
+        ("max_contexts", ctypes.c_int32),
+        ("host_pool_bytes", ctypes.c_uint64),
+        ("max_context_tokens", ctypes.c_int64),
+        ("shrink_mode", ctypes.c_int32),
+        ("pad_", ctypes.c_int32),
+    ]
+
+
+class KvPlannerCounters(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "steps", "reused_own", "took_free", "reclaimed_borrowed", "reclaimed_above_target",
+        "reclaimed_idle_contexts", "reclaimed_idle_pages", "shrunk_pages", "refused",
+        "copied_in")] + [("free_pages", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(
@@ -188,6 +217,31 @@ def _load():
     lib.kv_host_generation.argtypes = [vp, ctypes.c_uint64, u64p, ctypes.POINTER(ctypes.c_int64)]
     lib.kv_host_recycle.restype = i32
     lib.kv_host_recycle.argtypes = [vp, ctypes.c_uint64, u64p]
+    lib.kv_planner_create.restype = i32
+    lib.kv_planner_create.argtypes = [ctypes.POINTER(KvPlannerDesc), ctypes.POINTER(vp),
+                                      ctypes.c_char_p, sz]
+    lib.kv_planner_destroy.restype = i32
+    lib.kv_planner_destroy.argtypes = [vp]
+    lib.kv_planner_info.restype = i32
+    lib.kv_planner_info.argtypes = [vp, ctypes.POINTER(ctypes.c_int64),
+                                    ctypes.POINTER(ctypes.c_int), ctypes.c_char_p, sz]
+    lib.kv_planner_admit.restype = i32
+    lib.kv_planner_admit.argtypes = [vp, ctypes.c_uint64, i32, i32]
+    lib.kv_planner_set_target.restype = i32
+    lib.kv_planner_set_target.argtypes = [vp, ctypes.c_uint64, i32, i32]
+    lib.kv_planner_release.restype = i32
+    lib.kv_planner_release.argtypes = [vp, ctypes.c_uint64]
+    lib.kv_planner_step.restype = i32
+    lib.kv_planner_step.argtypes = [vp, u64p, ctypes.POINTER(ctypes.c_int64), i32,
+                                    ctypes.POINTER(ctypes.c_int32)]
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    lib.kv_planner_resident.restype = i32
+    lib.kv_planner_resident.argtypes = [vp, ctypes.c_uint64, i32p, i32p, i32,
+                                        ctypes.POINTER(ctypes.c_int)]
+    lib.kv_planner_copied.restype = i32
+    lib.kv_planner_copied.argtypes = [vp, ctypes.c_uint64, i32p, i32, ctypes.POINTER(ctypes.c_int)]
+    lib.kv_planner_get_counters.restype = i32
+    lib.kv_planner_get_counters.argtypes = [vp, ctypes.POINTER(KvPlannerCounters)]
     return lib
 
 
@@ -473,6 +527,86 @@ class Arena:
     def close(self):
         if self.handle:
             lib.kv_arena_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class Planner:
+    """Owner of a kv_planner handle (admission and device-window bookkeeping)."""
+
+    def __init__(self, pool_gib: int, n_layers: int = 16, row_bytes: int = 4096,
+                 page_tokens: int = PAGE_TOKENS, sink_pages: int = 1, max_contexts: int = 8,
+                 host_pool_bytes: int = 1 << 40, max_context_tokens: int = 131072,
+                 shrink_mode: bool = False):
+        d = KvPlannerDesc()
+        d.pool_gib = pool_gib
+        d.n_layers = n_layers
+        d.row_bytes = row_bytes
+        d.page_tokens = page_tokens
+        d.sink_pages = sink_pages
+        d.max_contexts = max_contexts
+        d.host_pool_bytes = host_pool_bytes
+        d.max_context_tokens = max_context_tokens
+        d.shrink_mode = 1 if shrink_mode else 0
+        h = ctypes.c_void_p()
+        buf = ctypes.create_string_buffer(1024)
+        self.handle = None
+        _check(lib.kv_planner_create(ctypes.byref(d), ctypes.byref(h), buf, 1024))
+        self.handle = h
+        self.formula = buf.value.decode()
+
+    def info(self):
+        n = ctypes.c_int64()
+        c = ctypes.c_int()
+        _check(lib.kv_planner_info(self.handle, ctypes.byref(n), ctypes.byref(c), None, 0))
+        return n.value, c.value
+
+    def admit(self, ctx: int, target: int, burst: int = 0):
+        _check(lib.kv_planner_admit(self.handle, ctx, target, burst))
+
+    def set_target(self, ctx: int, target: int, burst: int = 0):
+        _check(lib.kv_planner_set_target(self.handle, ctx, target, burst))
+
+    def release(self, ctx: int):
+        _check(lib.kv_planner_release(self.handle, ctx))
+
+    def step(self, contexts) -> list:
+        """contexts: list of (ctx, length_tokens).  Returns admitted flags."""
+        n = len(contexts)
+        ids = (ctypes.c_uint64 * max(1, n))(*[c for c, _ in contexts])
+        lens = (ctypes.c_int64 * max(1, n))(*[L for _, L in contexts])
+        adm = (ctypes.c_int32 * max(1, n))()
+        _check(lib.kv_planner_step(self.handle, ids, lens, n, adm))
+        return [bool(adm[i]) for i in range(n)]
+
+    def resident(self, ctx: int) -> dict:
+        n = ctypes.c_int()
+        _check(lib.kv_planner_resident(self.handle, ctx, None, None, 0, ctypes.byref(n)))
+        lg = (ctypes.c_int32 * max(1, n.value))()
+        pl = (ctypes.c_int32 * max(1, n.value))()
+        _check(lib.kv_planner_resident(self.handle, ctx, lg, pl, n.value, ctypes.byref(n)))
+        return {lg[i]: pl[i] for i in range(n.value)}
+
+    def copied(self, ctx: int) -> list:
+        n = ctypes.c_int()
+        _check(lib.kv_planner_copied(self.handle, ctx, None, 0, ctypes.byref(n)))
+        lg = (ctypes.c_int32 * max(1, n.value))()
+        _check(lib.kv_planner_copied(self.handle, ctx, lg, n.value, ctypes.byref(n)))
+        return [lg[i] for i in range(n.value)]
+
+    def counters(self) -> dict:
+        c = KvPlannerCounters()
+        _check(lib.kv_planner_get_counters(self.handle, ctypes.byref(c)))
+        return c.as_dict()
+
+    def close(self):
+        if self.handle:
+            lib.kv_planner_destroy(self.handle)
             self.handle = None
 
     def __del__(self):

@@ -24,7 +24,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedattn.so")
 
-SOURCES = ["common.cpp", "decode_attn.cu", "lse_merge.cu", "arena.cu"]
+SOURCES = ["common.cpp", "decode_attn.cu", "lse_merge.cu", "arena.cu", "planner.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
           "-Xcompiler", "-Wall"]
