@@ -335,7 +335,6 @@ extern "C" int kv_planner_step(kv_planner* P, const uint64_t* ctx_ids, const int
       c.pages[lp] = pool;
       if (!taken_from_window && (int)held > c.target) c.borrowed += 1;
       c.copied.push_back(lp);
-      P->c.copied_in += 1;
     }
     for (int32_t p : desired)
       if (!c.pages.count(p)) P->c.shrunk_pages += 1;
@@ -346,6 +345,16 @@ extern "C" int kv_planner_step(kv_planner* P, const uint64_t* ctx_ids, const int
     c.refused = !ok;
     if (!ok) P->c.refused += 1;
     if (admitted) admitted[i] = ok ? 1 : 0;
+  }
+  // A page made hot for one context may have been reclaimed by a later one
+  // in the same step: only pages still resident at the boundary are copied.
+  for (int i = 0; i < n; ++i) {
+    Ctx& c = P->ctxs[ctx_ids[i]];
+    std::vector<int32_t> kept;
+    for (int32_t lp : c.copied)
+      if (c.pages.count(lp)) kept.push_back(lp);
+    c.copied.swap(kept);
+    P->c.copied_in += c.copied.size();
   }
   return PA_OK;
 }

@@ -275,3 +275,139 @@ class StagedDecode:
 
     def close(self):
         self.handle.close()
+
+
+class PlannedDecode:
+    """Decode steps whose device window follows the admission planner.
+
+    The arena holds, per layer, one region of the planner's pool pages (pool
+    page p of layer l is arena page l * pool_pages + p) followed by the
+    staging slots.  At each step the planner decides every context's hot
+    pages ("Staging without a stall", section "Admission that does
+    arithmetic"); pages that turned hot are copied in once from pinned host
+    memory (after the previous step's attention and write-back are done with
+    the pool pages they reuse), and each layer stages every page that is not
+    hot.  Contexts are the workload's requests; all run every step.
+    """
+
+    def __init__(self, w: DecodeWorkload, t: dict, host: HostHistory, planner,
+                 targets, bursts, n_slots: int = 2, compute_stream=None):
+        geo = w.geometry
+        self.w, self.t, self.host, self.planner = w, t, host, planner
+        self.n_layers = t["pool"].shape[0]
+        dev = t["pool"].device
+        self.dev = dev
+        self.compute = compute_stream or torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.pool_pages, _ = planner.info()
+        self.win_pages = self.n_layers * self.pool_pages
+        self.slot_pages = max(1, sum(w.pages_of(r) for r in range(w.batch)))
+        arena_pages = self.win_pages + n_slots * self.slot_pages
+        self.arena = torch.full((arena_pages, geo.page_tokens, geo.row_elems), float("nan"),
+                                dtype=torch.bfloat16, device=dev)
+        self.page_tables = torch.zeros((n_slots, w.batch, w.max_pages), dtype=torch.int32,
+                                       device=dev)
+        torch.cuda.synchronize(dev)
+        self.handle = B.Arena(self.arena.data_ptr(), self.arena.numel() * 2, geo.row_bytes,
+                              n_slots, self.win_pages, self.slot_pages,
+                              self.page_tables.data_ptr(), w.batch, w.max_pages,
+                              compute_stream=self.compute, h2d_stream=self.h2d,
+                              d2h_stream=self.d2h)
+        for r in range(w.batch):
+            planner.admit(r, int(targets[r]), int(bursts[r]))
+        self.step_done = torch.cuda.Event()
+        self.wb_done = torch.cuda.Event()
+        self.have_prev = False
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.workspace = B.alloc_workspace(w.batch, 1, geo.n_q_heads, geo.n_kv_heads,
+                                           geo.head_dim, device=dev)
+        self.out = torch.empty((self.n_layers, w.batch, geo.n_q_heads, geo.head_dim),
+                               dtype=torch.float32, device=dev)
+        self.lse = torch.empty((self.n_layers, w.batch, geo.n_q_heads), dtype=torch.float32,
+                               device=dev)
+        self.tile_out = torch.empty((self.n_layers, w.batch, 1, geo.n_q_heads, geo.head_dim),
+                                    dtype=torch.float32, device=dev)
+        self.tile_lse = torch.empty((self.n_layers, w.batch, 1, geo.n_q_heads),
+                                    dtype=torch.float32, device=dev)
+        self.part_offsets = torch.arange(0, w.batch + 1, dtype=torch.int32, device=dev)
+        self.resident = [dict() for _ in range(w.batch)]
+
+    def _copy_in(self, lengths):
+        """Copy the pages that turned hot into their pool pages, every layer."""
+        geo = self.w.geometry
+        pt = geo.page_tokens
+        if self.have_prev:
+            self.h2d.wait_event(self.step_done)
+            self.h2d.wait_event(self.wb_done)
+        with torch.cuda.stream(self.h2d):
+            for r in range(self.w.batch):
+                res = self.resident[r]
+                for lp in self.planner.copied(r):
+                    lo = lp * pt
+                    hi = min(int(lengths[r]) - 1, lo + pt)   # the new row comes from append
+                    if hi <= lo:
+                        continue
+                    for i in range(self.n_layers):
+                        page = i * self.pool_pages + res[lp]
+                        src = self.host.rows[self.host.offsets[(i, r)] + lo:
+                                             self.host.offsets[(i, r)] + hi]
+                        self.arena[page, : hi - lo].copy_(src, non_blocking=True)
+
+    def _runs(self, i, r, L):
+        """Page runs of request r for layer i: hot pages from the pool,
+        maximal runs of cold pages staged from the host."""
+        pt = self.w.geometry.page_tokens
+        n = -(-L // pt)
+        res = self.resident[r]
+        runs, lp = [], 0
+        while lp < n:
+            if lp in res:
+                runs.append(dict(logical_page=lp, n_pages=1,
+                                 resident_page=i * self.pool_pages + res[lp]))
+                lp += 1
+                continue
+            start = lp
+            while lp < n and lp not in res:
+                lp += 1
+            rows = min(lp * pt, L - 1) - start * pt
+            runs.append(dict(logical_page=start, n_pages=lp - start, n_rows=max(0, rows),
+                             host_rows=self.host.row_address(i, r, start * pt)))
+        return runs
+
+    def step(self, lengths):
+        """One decode step at the given lengths (tokens, including the new one)."""
+        w, t, geo = self.w, self.t, self.w.geometry
+        admitted = self.planner.step([(r, int(lengths[r])) for r in range(w.batch)])
+        if not all(admitted):
+            raise RuntimeError(f"planner refused contexts {admitted}")
+        self.resident = [self.planner.resident(r) for r in range(w.batch)]
+        self._copy_in(lengths)
+        tiles = np.zeros((w.batch, 1, 2), dtype=np.int32)
+        tiles[:, 0, 1] = lengths
+        for i in range(self.n_layers):
+            reqs = [(r, (i << 32) | r, self._runs(i, r, int(lengths[r])))
+                    for r in range(w.batch)]
+            slot, _ = self.handle.stage_layer(i, reqs)
+            table = self.page_tables[slot]
+            B.kv_append_rows(self.arena, table, t["positions"], t["new_rows"][i],
+                             status=self.status, stream=self.compute)
+            B.paged_decode_attn_lse(t["q"][i], self.arena, table, tiles, geo.scale,
+                                    self.tile_out[i], self.tile_lse[i], self.workspace,
+                                    stream=self.compute)
+            B.lse_merge(self.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
+                        self.tile_lse[i].view(-1, geo.n_q_heads), self.part_offsets,
+                        self.out[i], self.lse[i], stream=self.compute)
+            self.handle.mark_attention_done(i)
+            self.handle.writeback_tail(
+                i, [(r, int(lengths[r]) - 1, self.host.row_address(i, r, int(lengths[r]) - 1),
+                     (i << 32) | r) for r in range(w.batch)])
+        self.step_done.record(self.compute)
+        self.wb_done.record(self.d2h)
+        self.have_prev = True
+
+    def kernel_status(self) -> int:
+        return int(self.workspace[:4].view(torch.int32).item()) | int(self.status.item())
+
+    def close(self):
+        self.handle.close()

@@ -160,6 +160,18 @@ def test_shrink_keeps_the_tail_hot_and_refuses_below_the_floor(B):
     assert p.counters()["shrunk_pages"] == 10 + 4
 
 
+def test_copied_pages_are_those_still_hot_at_the_step_boundary(B):
+    p = planner(B, 1)                                               # 256 pool pages
+    p.admit(1, target=100, burst=156)
+    p.admit(2, target=100)
+    ok = p.step([(1, pages(300)), (2, pages(100))])                 # 2 reclaims 1's borrowed pages
+    assert ok == [True, True]
+    res1 = p.resident(1)
+    assert len(res1) == 156 and len(p.resident(2)) == 100
+    assert sorted(p.copied(1)) == sorted(res1)                      # not the 100 taken back
+    assert p.counters()["copied_in"] == 256
+
+
 def test_release_returns_every_page(B):
     p = planner(B, 1)
     p.admit(1, target=40)
