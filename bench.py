@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cuda-core", action="store_true",
                     help="time the CUDA-core attention kernel instead of the tensor-core one")
+    ap.add_argument("--unfused", action="store_true",
+                    help="issue the tail write and the attention as two launches per layer")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-workers", type=int, default=0)
@@ -315,16 +317,26 @@ def run_ours(args):
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_ev)]
 
+    fused = not (args.cuda_core or args.unfused)
+    launches_per_step = (2 if fused else 3) * w.n_layers
+
     def resident_step(step_idx, s):
         o = res.o
         for i in range(w.n_layers):
-            B.kv_append_rows(t["pool"][i], t["page_table"], t["positions"], t["new_rows"][i],
-                             status=res.status, stream=s)
+            if not fused:
+                B.kv_append_rows(t["pool"][i], t["page_table"], t["positions"],
+                                 t["new_rows"][i], status=res.status, stream=s)
             if step_idx is not None:
                 ev[step_idx * w.n_layers + i][0].record(s)
-            B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], res.tiles,
-                                    geo.scale, o.tile_out[i], o.tile_lse[i], res.workspace,
-                                    stream=s, cuda_core=args.cuda_core)
+            if fused:
+                B.paged_decode_attn_lse_append(t["q"][i], t["pool"][i], t["page_table"],
+                                               res.tiles, geo.scale, t["positions"],
+                                               t["new_rows"][i], o.tile_out[i], o.tile_lse[i],
+                                               res.workspace, stream=s)
+            else:
+                B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], res.tiles,
+                                        geo.scale, o.tile_out[i], o.tile_lse[i], res.workspace,
+                                        stream=s, cuda_core=args.cuda_core)
             if step_idx is not None:
                 ev[step_idx * w.n_layers + i][1].record(s)
             B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
@@ -403,11 +415,12 @@ def run_ours(args):
                        "route": "resident", "parallelism": f"replicas x{world}",
                        "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step)",
                        "kernel": "cuda-core fp32" if args.cuda_core
-                       else "tensor-core mma.sync bf16 + TMA pipeline",
+                       else "tensor-core mma.sync bf16 + TMA pipeline"
+                       + (", tail write fused" if fused else ""),
                        "accumulate": "fp32"},
             "tokens_per_s": round(tokens_per_s, 1),
             "pct_of_hbm_peak": round(100 * value / peak, 2),
-            "gpu_launches": 3 * w.n_layers * args.steps,
+            "gpu_launches": launches_per_step * args.steps,
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
@@ -417,7 +430,8 @@ def run_ours(args):
                          "mean_launch_ms": round(kern_ms, 5)},
             "clocks": clk,
             "host_issue_ms_per_step": round(1e3 * host_issue_s / args.steps, 4),
-            "step_launch": "CUDA graph of the 48 launches of one step, replayed per step",
+            "step_launch": f"CUDA graph of the {launches_per_step} launches of one step, "
+                           "replayed per step",
         }
         if e2e is not None:
             line["e2e"] = e2e

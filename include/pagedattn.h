@@ -171,6 +171,31 @@ int paged_decode_attn_lse_noalloc(const void* q, const void* pool, int64_t pool_
                                   float scale, float* out, float* lse,
                                   int32_t* status, cudaStream_t stream);
 
+/* paged_decode_attn_lse and kv_append_rows in one launch ([KVE-exact],
+ * [SWS-lease]): the step's new token of each request is written into its page
+ * AND attended, so the pool does not have to hold the row before the call.
+ *
+ *   All arguments as for paged_decode_attn_lse, except:
+ *   pool       writable: row new_rows[b] is stored at the pool row of token
+ *              positions[b] of request b (page page_table[b][positions[b]/64],
+ *              row positions[b] % 64), as kv_append_rows stores it.
+ *   positions  device int32 [B].
+ *   new_rows   device bf16 [B][2*n_kv_heads*head_dim] (K heads, then V
+ *              heads), 16-byte aligned.
+ * Every tile that covers positions[b] uses new_rows[b] for that token, whatever
+ * the pool held there, so outputs are bit-identical to kv_append_rows followed
+ * by paged_decode_attn_lse on the same stream.  An out-of-range position or
+ * page id skips the store and ORs PA_STATUS_BAD_ROW into the workspace status
+ * word.  No other call may read or write that pool row while this one runs. */
+int paged_decode_attn_lse_append(const void* q, void* pool, int64_t pool_pages,
+                                 const int32_t* page_table, int max_pages,
+                                 const int32_t* tiles, int B, int T,
+                                 int n_q_heads, int n_kv_heads, int head_dim,
+                                 float scale, const int32_t* positions,
+                                 const void* new_rows, float* out, float* lse,
+                                 void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ */
 /* FP32 LSE merge  ([KVE-exact])                                            */
 /* ------------------------------------------------------------------------ */

@@ -34,7 +34,8 @@ PAGE_TOKENS = 64
 EXPORTED = [
     "kv_last_error", "pa_version",
     "paged_decode_attn_lse_workspace_bytes", "paged_decode_attn_lse",
-    "paged_decode_attn_lse_cuda_core", "paged_decode_attn_lse_noalloc", "lse_merge",
+    "paged_decode_attn_lse_cuda_core", "paged_decode_attn_lse_noalloc",
+    "paged_decode_attn_lse_append", "lse_merge",
     "kv_append_rows",
     "kv_arena_create", "kv_arena_destroy", "kv_arena_drain", "kv_stage_layer",
     "kv_mark_attention_done", "kv_writeback_tail", "kv_arena_get_stats",
@@ -179,6 +180,9 @@ def _load():
     lib.paged_decode_attn_lse_noalloc.restype = i32
     lib.paged_decode_attn_lse_noalloc.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32,
                                                   i32, ctypes.c_float, vp, vp, vp, vp]
+    lib.paged_decode_attn_lse_append.restype = i32
+    lib.paged_decode_attn_lse_append.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32,
+                                                 i32, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp]
     lib.lse_merge.restype = i32
     lib.lse_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
     lib.kv_append_rows.restype = i32
@@ -336,6 +340,31 @@ def paged_decode_attn_lse_noalloc(q, pool, page_table, tiles, scale, out, lse, s
         Hq, n_kv, D, float(scale), _dev(out, torch.float32, "out"),
         _dev(lse, torch.float32, "lse"),
         None if status is None else _dev(status, torch.int32, "status"), _stream_handle(stream)))
+
+
+def paged_decode_attn_lse_append(q, pool, page_table, tiles, scale, positions, new_rows, out,
+                                 lse, workspace, stream=None, pool_pages=None):
+    """kv_append_rows and paged_decode_attn_lse in one launch: new_rows bf16
+    [B][2*Hkv*D] are stored at token positions int32 [B] (device) of each
+    request's pages and attended in place of whatever the pool held there."""
+    B, Hq, D = q.shape
+    row_elems = pool.shape[-1]
+    n_kv = row_elems // (2 * D)
+    arr, tiles_ptr = _host_tiles(tiles)
+    T = arr.shape[1]
+    if arr.shape[0] != B:
+        raise ValueError("tiles must be [B][T][2]")
+    if tuple(new_rows.shape) != (B, row_elems) or tuple(positions.shape) != (B,):
+        raise ValueError("new_rows must be [B][2*Hkv*D] and positions [B]")
+    if pool_pages is None:
+        pool_pages = pool.numel() // (PAGE_TOKENS * row_elems)
+    _check(lib.paged_decode_attn_lse_append(
+        _dev(q, torch.bfloat16, "q"), _dev(pool, torch.bfloat16, "pool", False), int(pool_pages),
+        _dev(page_table, torch.int32, "page_table"), int(page_table.shape[1]), tiles_ptr, B, T,
+        Hq, n_kv, D, float(scale), _dev(positions, torch.int32, "positions"),
+        _dev(new_rows, torch.bfloat16, "new_rows"), _dev(out, torch.float32, "out"),
+        _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"),
+        workspace.numel(), _stream_handle(stream)))
 
 
 def lse_merge(out_parts, lse_parts, part_offsets, out, lse, stream=None):

@@ -115,6 +115,13 @@ struct Params {
   int n_units;
   int grid;
   float scale_log2;
+  // Optional new-token rows: row new_rows[b] is written to the pool at token
+  // positions[b] of request b, and attention uses it for that token.
+  __nv_bfloat16* pool;
+  const __nv_bfloat16* new_rows;
+  const int32_t* positions;
+  int n_requests;
+  int row_elems;
   Unit units[kMaxUnits];
 };
 
@@ -186,6 +193,16 @@ __device__ __forceinline__ Shared carve(uint8_t* raw) {
   return s;
 }
 
+// Writes `count` 16-byte chunks of a new row's K (or V) slice into row r of
+// a swizzled stage half (K at half_base, V at half_base + kHalfBytes): chunk
+// c (8 dims) goes to box c / 8, 16-byte position (c % 8) ^ (r % 8).
+__device__ __forceinline__ void put_row_chunk(uint32_t half_base, int r, int c, uint4 v) {
+  const uint32_t a = half_base + (c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4);
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
 // ---------------------------------------------------------------------------
 // Thread organisation.  Each page is split into kGroups groups of 16 tokens.
 // Tensor-core variant: 8 consumer warps; warp w takes token group w % 4 and
@@ -249,6 +266,26 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
   // Everything above touches only parameters and shared memory; from here on
   // the kernel reads what earlier kernels in the stream wrote.
   ptx::grid_dependency_wait();
+
+  // New-token rows: CTA b % grid writes request b's row into its page.  A
+  // CTA that streams that page may read it before or after this write, so
+  // every consumer substitutes the row in shared memory (below) instead.
+  if (p.new_rows != nullptr) {
+    for (int b = blockIdx.x; b < p.n_requests; b += p.grid) {
+      const int pos = p.positions[b];
+      const int lp = pos >= 0 ? pos / kPage : -1;
+      const long long page = (lp >= 0 && lp < p.max_pages)
+                                 ? (long long)p.page_table[(size_t)b * p.max_pages + lp] : -1;
+      if (page < 0 || page >= p.pool_pages) {
+        if (threadIdx.x == 0) atomicOr(p.status, PA_STATUS_BAD_ROW);
+        continue;
+      }
+      const uint4* src = reinterpret_cast<const uint4*>(p.new_rows + (size_t)b * p.row_elems);
+      uint4* dst = reinterpret_cast<uint4*>(p.pool + ((size_t)page * kPage + pos % kPage) *
+                                                         (size_t)p.row_elems);
+      for (int i = threadIdx.x; i < p.row_elems / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+    }
+  }
 
   const long long cta_start = (long long)blockIdx.x * p.total_pages / p.grid;
   const long long cta_end = (long long)(blockIdx.x + 1) * p.total_pages / p.grid;
@@ -359,6 +396,20 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     const int b = bt / p.T;
     const int first_page_tok = (U.tok_start / kPage) * kPage;
     int poisoned = 0;
+    // The new token of this request, if it falls in this segment's pages:
+    // its K slice (chunk `lane`) and V slice (chunk `lane`) of kv head g.
+    int sub_pos = -1;
+    uint4 sub_k = make_uint4(0u, 0u, 0u, 0u), sub_v = make_uint4(0u, 0u, 0u, 0u);
+    if (p.new_rows != nullptr) {
+      const int pos = p.positions[b];
+      if (pos >= max(U.tok_start, first_page_tok + lo * kPage) &&
+          pos < min(U.tok_end, first_page_tok + hi * kPage)) {
+        sub_pos = pos;
+        const uint4* row = reinterpret_cast<const uint4*>(p.new_rows + (size_t)b * p.row_elems);
+        sub_k = __ldg(row + (g * kD) / 8 + lane);
+        sub_v = __ldg(row + ((Hkv + g) * kD) / 8 + lane);
+      }
+    }
 
     float* xo_g = sh.xo + (tg * kMaxG) * kXRow;   // this token group's exchange rows
     float* xml_g = sh.xml + (tg * kMaxG) * 2;
@@ -410,6 +461,15 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         const int vhi = min(U.tok_end, page_tok + kPage);
         const int tb = page_tok + 16 * tg;
         const uint32_t stage = ptx::smem_addr(sh.stages + s * kStageBytes);
+        if (sub_pos >= tb && sub_pos < tb + 16) {
+          // The new token's row: both warps of the group write its K slice
+          // (same bytes), each its own half of the V slice.
+          const int r = sub_pos - page_tok;
+          put_row_chunk(stage, r, lane, sub_k);
+          if ((lane >> 4) == dh) put_row_chunk(stage + kHalfBytes, r, lane, sub_v);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+        }
         if (tb + 16 > vlo && tb < vhi) {
           if (tb < vlo || tb + 16 > vhi) {
             // Rows of this group outside the tile: zero this warp's half of
@@ -576,6 +636,13 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         const int vhi = min(U.tok_end, page_tok + kPage);
         const int tb = page_tok + 16 * tg;
         const uint32_t stage = ptx::smem_addr(sh.stages + s * kStageBytes);
+        if (sub_pos >= tb && sub_pos < tb + 16) {
+          const int r = sub_pos - page_tok;
+          put_row_chunk(stage, r, lane, sub_k);
+          put_row_chunk(stage + kHalfBytes, r, lane, sub_v);
+          ptx::fence_proxy_async_smem();
+          __syncwarp();
+        }
         const int r_lo = max(0, vlo - tb);
         const int r_hi = min(16, vhi - tb);
         for (int r = r_lo; r < r_hi; ++r) {
@@ -894,7 +961,8 @@ int launch_units(const CUtensorMap& tmap, const std::vector<Unit>& units, size_t
 int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
         const int32_t* page_table, int max_pages, const int32_t* tiles, int B, int T,
         int n_q_heads, int n_kv_heads, int head_dim, float scale, float* out, float* lse,
-        void* workspace, size_t ws_bytes, cudaStream_t stream) {
+        void* workspace, size_t ws_bytes, cudaStream_t stream,
+        const int32_t* positions = nullptr, const void* new_rows = nullptr) {
   clear_error();
   PA_REQUIRE(B >= 0 && T >= 0, "B and T must be >= 0 (got %d, %d)", B, T);
   if ((long long)B * T == 0) return PA_OK;
@@ -926,6 +994,10 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
                "tile %lld of request %lld is [%d, %d), outside [0, %lld]", i % T, i / T, s, e,
                max_tok);
   }
+  PA_REQUIRE((positions == nullptr) == (new_rows == nullptr),
+             "positions and new_rows go together");
+  PA_REQUIRE(new_rows == nullptr || reinterpret_cast<uintptr_t>(new_rows) % 16 == 0,
+             "new_rows must be 16-byte aligned");
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
 
@@ -976,6 +1048,10 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
   common.Hkv = n_kv_heads;
   common.G = G;
   common.scale_log2 = scale * kLog2e;
+  common.pool = static_cast<__nv_bfloat16*>(const_cast<void*>(pool));
+  common.new_rows = static_cast<const __nv_bfloat16*>(new_rows);
+  common.positions = positions;
+  common.row_elems = row_elems;
 
   // Launches of at most kMaxUnitsLarge units each; every launch partitions its
   // own pages and reuses the workspace after the previous one (same stream).
@@ -1007,6 +1083,7 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
       return fail(PA_ERR_INVALID, "internal: %d partial slots exceed the %zu reserved",
                   part_cursor, slots);
     const long long eff_total = total > 0 ? total : 1;
+    common.n_requests = u0 == 0 ? B : 0;   // new rows are stored by the first launch
     int rc;
     if (n <= (size_t)kMaxUnitsSmall) {
       rc = tensor_cores ? launch_units<kMaxUnitsSmall, true>(tmap, units, u0, n, eff_total, grid,
@@ -1044,6 +1121,21 @@ extern "C" int paged_decode_attn_lse(const void* q, const void* pool, int64_t po
   return pa::decode::run(true, q, pool, pool_pages, page_table, max_pages, tiles, B, T,
                          n_q_heads, n_kv_heads, head_dim, scale, out, lse, workspace,
                          workspace_bytes, stream);
+}
+
+extern "C" int paged_decode_attn_lse_append(const void* q, void* pool, int64_t pool_pages,
+                                            const int32_t* page_table, int max_pages,
+                                            const int32_t* tiles, int B, int T, int n_q_heads,
+                                            int n_kv_heads, int head_dim, float scale,
+                                            const int32_t* positions, const void* new_rows,
+                                            float* out, float* lse, void* workspace,
+                                            size_t workspace_bytes, cudaStream_t stream) {
+  pa::clear_error();
+  if (!positions || !new_rows)
+    return pa::fail(PA_ERR_INVALID, "positions and new_rows are required");
+  return pa::decode::run(true, q, pool, pool_pages, page_table, max_pages, tiles, B, T,
+                         n_q_heads, n_kv_heads, head_dim, scale, out, lse, workspace,
+                         workspace_bytes, stream, positions, new_rows);
 }
 
 extern "C" int paged_decode_attn_lse_cuda_core(const void* q, const void* pool,

@@ -1,13 +1,14 @@
 """One decode step of paged GQA attention over every layer, on two routes.
 
-Resident route: the whole history sits in a device pool; per layer the new
-token's row is written into its page, the attention kernel returns per-tile
-(out, LSE), and the FP32 merge combines the tiles.
+Resident route: the whole history sits in a device pool; per layer one
+launch writes the new token's row into its page and returns per-tile (out,
+LSE) with that row attended (``fused=False`` issues the tail write and the
+attention as two launches), and the FP32 merge combines the tiles.
 
 Staged route ("Staging without a stall"; "KV-cache engineering", section
 "Staging layers under a lease"): pinned host memory owns the history; per
 layer the arena copies the layer's non-resident pages into a device slot on
-the H2D stream, the compute stream waits on the copy's event, the same three
+the H2D stream, the compute stream waits on the copy's event, the same
 kernels run against the slot, attention is marked done, and only the new
 token's row is written back to its pinned host row on the D2H stream.
 
@@ -22,6 +23,22 @@ import torch
 
 from . import binding as B
 from .workloads import DecodeWorkload, history_rows
+
+
+def _layer_kernels(fused, cuda_core, q, pool, table, positions, new_row, tiles, scale, tile_out,
+                   tile_lse, workspace, status, part_offsets, out, lse, stream):
+    """The layer's kernels: tail write + attention (one fused launch, or two),
+    then the merge of the tiles."""
+    geo_h, geo_d = tile_out.shape[-2], tile_out.shape[-1]
+    if fused and not cuda_core:
+        B.paged_decode_attn_lse_append(q, pool, table, tiles, scale, positions, new_row,
+                                       tile_out, tile_lse, workspace, stream=stream)
+    else:
+        B.kv_append_rows(pool, table, positions, new_row, status=status, stream=stream)
+        B.paged_decode_attn_lse(q, pool, table, tiles, scale, tile_out, tile_lse, workspace,
+                                stream=stream, cuda_core=cuda_core)
+    B.lse_merge(tile_out.view(-1, geo_h, geo_d), tile_lse.view(-1, geo_h), part_offsets, out,
+                lse, stream=stream)
 
 
 class _Outputs:
@@ -43,10 +60,11 @@ class ResidentDecode:
     """Decode step over a device-resident pool [layers][pages][64][row_elems]."""
 
     def __init__(self, w: DecodeWorkload, t: dict, cuda_core: bool = False,
-                 tiles: np.ndarray | None = None, stream=None):
+                 tiles: np.ndarray | None = None, stream=None, fused: bool = True):
         self.w = w
         self.t = t
         self.cuda_core = cuda_core
+        self.fused = fused
         self.tiles = np.ascontiguousarray(w.tiles if tiles is None else tiles, dtype=np.int32)
         self.n_layers = t["pool"].shape[0]
         dev = t["pool"].device
@@ -63,16 +81,15 @@ class ResidentDecode:
 
     def layer(self, i: int, attention_only: bool = False):
         t, o, geo = self.t, self.o, self.w.geometry
-        if not attention_only:
-            B.kv_append_rows(t["pool"][i], t["page_table"], t["positions"], t["new_rows"][i],
-                             status=self.status, stream=self.stream)
-        B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], self.tiles, geo.scale,
-                                o.tile_out[i], o.tile_lse[i], self.workspace,
-                                stream=self.stream, cuda_core=self.cuda_core)
-        if not attention_only:
-            B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
-                        o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
-                        o.lse[i], stream=self.stream)
+        if attention_only:
+            B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], self.tiles,
+                                    geo.scale, o.tile_out[i], o.tile_lse[i], self.workspace,
+                                    stream=self.stream, cuda_core=self.cuda_core)
+            return
+        _layer_kernels(self.fused, self.cuda_core, t["q"][i], t["pool"][i], t["page_table"],
+                       t["positions"], t["new_rows"][i], self.tiles, geo.scale, o.tile_out[i],
+                       o.tile_lse[i], self.workspace, self.status, o.part_offsets, o.out[i],
+                       o.lse[i], self.stream)
 
     def step(self):
         for i in range(self.n_layers):
@@ -145,10 +162,11 @@ class StagedDecode:
 
     def __init__(self, w: DecodeWorkload, t: dict, host: HostHistory, n_slots: int = 2,
                  cuda_core: bool = False, compute_stream=None, h2d_stream=None,
-                 d2h_stream=None, leases: bool = False):
+                 d2h_stream=None, leases: bool = False, fused: bool = True):
         geo = w.geometry
         self.w, self.t, self.host, self.cuda_core = w, t, host, cuda_core
         self.leases = leases
+        self.fused = fused
         self.step_index = 0
         self.receipts = []
         self.n_layers = t["pool"].shape[0]
@@ -221,14 +239,10 @@ class StagedDecode:
 
     def _kernels(self, i: int, table):
         t, o, geo = self.t, self.o, self.w.geometry
-        B.kv_append_rows(self.arena, table, t["positions"], t["new_rows"][i], status=self.status,
-                         stream=self.compute)
-        B.paged_decode_attn_lse(t["q"][i], self.arena, table, self.tiles, geo.scale,
-                                o.tile_out[i], o.tile_lse[i], self.workspace,
-                                stream=self.compute, cuda_core=self.cuda_core)
-        B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
-                    o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i], o.lse[i],
-                    stream=self.compute)
+        _layer_kernels(self.fused, self.cuda_core, t["q"][i], self.arena, table, t["positions"],
+                       t["new_rows"][i], self.tiles, geo.scale, o.tile_out[i], o.tile_lse[i],
+                       self.workspace, self.status, o.part_offsets, o.out[i], o.lse[i],
+                       self.compute)
 
     def _lease_step(self):
         """One step as leases: begin, kernels, attention event, tail write-back
@@ -246,17 +260,8 @@ class StagedDecode:
         self.step_index += 1
 
     def layer(self, i: int):
-        t, o, geo = self.t, self.o, self.w.geometry
         slot, _ = self.handle.stage_layer(i, self.plan[i])
-        table = self.page_tables[slot]
-        B.kv_append_rows(self.arena, table, t["positions"], t["new_rows"][i], status=self.status,
-                         stream=self.compute)
-        B.paged_decode_attn_lse(t["q"][i], self.arena, table, self.tiles, geo.scale,
-                                o.tile_out[i], o.tile_lse[i], self.workspace,
-                                stream=self.compute, cuda_core=self.cuda_core)
-        B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
-                    o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i], o.lse[i],
-                    stream=self.compute)
+        self._kernels(i, self.page_tables[slot])
         self.handle.mark_attention_done(i)
         self.handle.writeback_tail(i, self.tails[i])
 
@@ -291,9 +296,10 @@ class PlannedDecode:
     """
 
     def __init__(self, w: DecodeWorkload, t: dict, host: HostHistory, planner,
-                 targets, bursts, n_slots: int = 2, compute_stream=None):
+                 targets, bursts, n_slots: int = 2, compute_stream=None, fused: bool = True):
         geo = w.geometry
         self.w, self.t, self.host, self.planner = w, t, host, planner
+        self.fused = fused
         self.n_layers = t["pool"].shape[0]
         dev = t["pool"].device
         self.dev = dev
@@ -389,15 +395,10 @@ class PlannedDecode:
             reqs = [(r, (i << 32) | r, self._runs(i, r, int(lengths[r])))
                     for r in range(w.batch)]
             slot, _ = self.handle.stage_layer(i, reqs)
-            table = self.page_tables[slot]
-            B.kv_append_rows(self.arena, table, t["positions"], t["new_rows"][i],
-                             status=self.status, stream=self.compute)
-            B.paged_decode_attn_lse(t["q"][i], self.arena, table, tiles, geo.scale,
-                                    self.tile_out[i], self.tile_lse[i], self.workspace,
-                                    stream=self.compute)
-            B.lse_merge(self.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
-                        self.tile_lse[i].view(-1, geo.n_q_heads), self.part_offsets,
-                        self.out[i], self.lse[i], stream=self.compute)
+            _layer_kernels(self.fused, False, t["q"][i], self.arena, self.page_tables[slot],
+                           t["positions"], t["new_rows"][i], tiles, geo.scale, self.tile_out[i],
+                           self.tile_lse[i], self.workspace, self.status, self.part_offsets,
+                           self.out[i], self.lse[i], self.compute)
             self.handle.mark_attention_done(i)
             self.handle.writeback_tail(
                 i, [(r, int(lengths[r]) - 1, self.host.row_address(i, r, int(lengths[r]) - 1),

@@ -90,3 +90,17 @@ def test_merge_and_append_argument_checks(B):
         B.PA_ERR_INVALID
     assert B.lib.kv_append_rows(fake, 4, fake, 4, fake, fake + 8, 1, 4096, None, None) == \
         B.PA_ERR_INVALID
+
+
+def test_fused_append_argument_checks(B):
+    fake = 1 << 20
+    arr = np.ascontiguousarray(np.asarray([[[0, 64]]], dtype=np.int32))
+
+    def call(positions, rows):
+        return B.lib.paged_decode_attn_lse_append(fake, fake, 16, fake, 8, arr.ctypes.data, 1, 1,
+                                                  24, 4, 256, 0.0625, positions, rows, fake, fake,
+                                                  fake, 1 << 30, None)
+    assert call(None, fake) == B.PA_ERR_INVALID
+    assert call(fake, None) == B.PA_ERR_INVALID
+    assert call(fake, fake + 8) == B.PA_ERR_INVALID
+    assert "new_rows" in B.last_error()
