@@ -59,6 +59,8 @@ def parse_args():
                     help="time the CUDA-core attention kernel instead of the tensor-core one")
     ap.add_argument("--unfused", action="store_true",
                     help="issue the tail write and the attention as two launches per layer")
+    ap.add_argument("--no-early-kv", action="store_true",
+                    help="make each launch wait for the previous kernel before loading pages")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-workers", type=int, default=0)
@@ -318,7 +320,12 @@ def run_ours(args):
           for _ in range(n_ev)]
 
     fused = not (args.cuda_core or args.unfused)
-    launches_per_step = (2 if fused else 3) * w.n_layers
+    # Within the step the pool and page table are written only by the step's
+    # own fused launches (layer i's launch stores layer i's new row), so each
+    # launch may load its first pages while the previous kernel finishes.
+    kv_ready = fused and not args.no_early_kv
+    merge = w.n_tiles > 1       # one tile per request: the merge is the identity
+    launches_per_step = (1 + int(merge) + int(not fused)) * w.n_layers
 
     def resident_step(step_idx, s):
         o = res.o
@@ -332,17 +339,19 @@ def run_ours(args):
                 B.paged_decode_attn_lse_append(t["q"][i], t["pool"][i], t["page_table"],
                                                res.tiles, geo.scale, t["positions"],
                                                t["new_rows"][i], o.tile_out[i], o.tile_lse[i],
-                                               res.workspace, stream=s)
+                                               res.workspace, stream=s, kv_ready=kv_ready)
             else:
                 B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], res.tiles,
                                         geo.scale, o.tile_out[i], o.tile_lse[i], res.workspace,
                                         stream=s, cuda_core=args.cuda_core)
             if step_idx is not None:
                 ev[step_idx * w.n_layers + i][1].record(s)
-            B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
-                        o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
-                        o.lse[i], stream=s)
+            if merge:
+                B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
+                            o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
+                            o.lse[i], stream=s)
 
+    torch.cuda.synchronize(dev)      # inputs written by torch kernels are complete
     for _ in range(max(3, args.warmup)):
         resident_step(None, stream)
     torch.cuda.synchronize(dev)
@@ -416,7 +425,8 @@ def run_ours(args):
                        "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step)",
                        "kernel": "cuda-core fp32" if args.cuda_core
                        else "tensor-core mma.sync bf16 + TMA pipeline"
-                       + (", tail write fused" if fused else ""),
+                       + (", tail write fused" if fused else "")
+                       + (", early page loads" if kv_ready else ""),
                        "accumulate": "fp32"},
             "tokens_per_s": round(tokens_per_s, 1),
             "pct_of_hbm_peak": round(100 * value / peak, 2),
@@ -463,10 +473,27 @@ def run_e2e(args, w, t, dev, D, B):
         out_host.copy_(st.o.out, non_blocking=True)
         lse_host.copy_(st.o.lse, non_blocking=True)
 
+    # host-link probe: the first layer's host history copied H2D on one stream
+    seg = host.rows[: sum(int(L) for L in w.lengths)]
+    dst = torch.empty(seg.shape, dtype=seg.dtype, device=dev)
+    ps = torch.cuda.Stream(dev)
+
+    def link_probe():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(ps):
+            dst.copy_(seg, non_blocking=True)
+            e0.record(ps)
+            for _ in range(3):
+                dst.copy_(seg, non_blocking=True)
+            e1.record(ps)
+        torch.cuda.synchronize(dev)
+        return 3 * seg.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
+
     for _ in range(max(3, args.warmup)):
         step()
     st.drain()
     torch.cuda.synchronize(dev)
+    probe_before = link_probe()
     steps = max(3, min(args.steps, 10))
     t0 = time.perf_counter()
     for _ in range(steps):
@@ -478,19 +505,7 @@ def run_e2e(args, w, t, dev, D, B):
         raise RuntimeError("staged route kernel status non-zero")
     stats = st.handle.stats()
     staged_per_step = stats.staged_bytes // stats.stage_generation * w.n_layers
-    # host-link probe: the first layer's host history copied H2D on one stream
-    seg = host.rows[: sum(int(L) for L in w.lengths)]
-    dst = torch.empty(seg.shape, dtype=seg.dtype, device=dev)
-    ps = torch.cuda.Stream(dev)
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(ps):
-        dst.copy_(seg, non_blocking=True)
-        e0.record(ps)
-        for _ in range(3):
-            dst.copy_(seg, non_blocking=True)
-        e1.record(ps)
-    torch.cuda.synchronize(dev)
-    probe_gbs = 3 * seg.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
+    probe_after = link_probe()
     del dst
     h2d = q_host.numel() * 2 + rows_host.numel() * 2 + staged_per_step
     d2h = out_host.numel() * 4 + lse_host.numel() * 4 + w.n_layers * w.batch * geo.row_bytes
@@ -500,7 +515,9 @@ def run_e2e(args, w, t, dev, D, B):
            "route": "host-staged, 2 arena slots, tail write-back",
            "ms_per_step": round(1e3 * secs / steps, 3),
            "h2d_GBps": round(staged_per_step * steps / secs / 1e9, 2),
-           "link_probe_h2d_GBps": round(probe_gbs, 2), "steps": steps, "_secs": secs}
+           "link_probe_h2d_GBps": [round(probe_before, 2), round(probe_after, 2)],
+           "link_probe": "one stream, before and after the timed steps",
+           "steps": steps, "_secs": secs}
     st.close()
     host.close()
     return res

@@ -186,7 +186,18 @@ int paged_decode_attn_lse_noalloc(const void* q, const void* pool, int64_t pool_
  * the pool held there, so outputs are bit-identical to kv_append_rows followed
  * by paged_decode_attn_lse on the same stream.  An out-of-range position or
  * page id skips the store and ORs PA_STATUS_BAD_ROW into the workspace status
- * word.  No other call may read or write that pool row while this one runs. */
+ * word.  No other call may read or write that pool row while this one runs.
+ *   flags      0 or PA_DECODE_KV_READY.  The kernels of this library start
+ *              under programmatic dependent launch: without the flag a launch
+ *              reads nothing in memory until the kernels before it in the
+ *              stream are complete.  PA_DECODE_KV_READY promises that the
+ *              page table and the pool rows this call reads are written by no
+ *              kernel that can still be running when this call's kernel
+ *              starts (the kernel just before it in the stream, or one chained
+ *              to that kernel by programmatic dependent launch); each CTA may
+ *              then load its first pages while those kernels finish.  Results
+ *              are the same with or without it when the promise holds. */
+#define PA_DECODE_KV_READY 1u
 int paged_decode_attn_lse_append(const void* q, void* pool, int64_t pool_pages,
                                  const int32_t* page_table, int max_pages,
                                  const int32_t* tiles, int B, int T,
@@ -194,7 +205,7 @@ int paged_decode_attn_lse_append(const void* q, void* pool, int64_t pool_pages,
                                  float scale, const int32_t* positions,
                                  const void* new_rows, float* out, float* lse,
                                  void* workspace, size_t workspace_bytes,
-                                 cudaStream_t stream);
+                                 unsigned flags, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ */
 /* FP32 LSE merge  ([KVE-exact])                                            */

@@ -28,6 +28,7 @@ PA_STATUS_BAD_PAGE = 1
 PA_STATUS_TIMEOUT = 2
 PA_STATUS_BAD_ROW = 4
 PA_ARENA_RECORD_ONLY = 1
+PA_DECODE_KV_READY = 1
 PAGE_TOKENS = 64
 
 # Every symbol pagedattn.h declares.
@@ -182,7 +183,8 @@ def _load():
                                                   i32, ctypes.c_float, vp, vp, vp, vp]
     lib.paged_decode_attn_lse_append.restype = i32
     lib.paged_decode_attn_lse_append.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32,
-                                                 i32, ctypes.c_float, vp, vp, vp, vp, vp, sz, vp]
+                                                 i32, ctypes.c_float, vp, vp, vp, vp, vp, sz,
+                                                 ctypes.c_uint, vp]
     lib.lse_merge.restype = i32
     lib.lse_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
     lib.kv_append_rows.restype = i32
@@ -343,10 +345,11 @@ def paged_decode_attn_lse_noalloc(q, pool, page_table, tiles, scale, out, lse, s
 
 
 def paged_decode_attn_lse_append(q, pool, page_table, tiles, scale, positions, new_rows, out,
-                                 lse, workspace, stream=None, pool_pages=None):
+                                 lse, workspace, stream=None, pool_pages=None, kv_ready=False):
     """kv_append_rows and paged_decode_attn_lse in one launch: new_rows bf16
     [B][2*Hkv*D] are stored at token positions int32 [B] (device) of each
-    request's pages and attended in place of whatever the pool held there."""
+    request's pages and attended in place of whatever the pool held there.
+    ``kv_ready`` passes PA_DECODE_KV_READY (see pagedattn.h for the promise)."""
     B, Hq, D = q.shape
     row_elems = pool.shape[-1]
     n_kv = row_elems // (2 * D)
@@ -364,7 +367,7 @@ def paged_decode_attn_lse_append(q, pool, page_table, tiles, scale, positions, n
         Hq, n_kv, D, float(scale), _dev(positions, torch.int32, "positions"),
         _dev(new_rows, torch.bfloat16, "new_rows"), _dev(out, torch.float32, "out"),
         _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"),
-        workspace.numel(), _stream_handle(stream)))
+        workspace.numel(), PA_DECODE_KV_READY if kv_ready else 0, _stream_handle(stream)))
 
 
 def lse_merge(out_parts, lse_parts, part_offsets, out, lse, stream=None):

@@ -122,6 +122,10 @@ struct Params {
   const int32_t* positions;
   int n_requests;
   int row_elems;
+  // The page table and the pool rows read are final before the kernel that
+  // precedes this one in the stream runs: the producer may issue its first
+  // kStages page loads before the grid dependency wait.
+  int kv_ready;
   Unit units[kMaxUnits];
 };
 
@@ -264,13 +268,17 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
   if (warp == kConsumerWarps && lane == 0) ptx::prefetch_tensormap(&tmap);
   __syncthreads();
   // Everything above touches only parameters and shared memory; from here on
-  // the kernel reads what earlier kernels in the stream wrote.
-  ptx::grid_dependency_wait();
+  // the kernel reads what earlier kernels in the stream wrote.  With kv_ready
+  // the producer warp defers this wait until its ring is full (below).
+  const bool early_kv = p.kv_ready != 0 && warp == kConsumerWarps;
+  if (!early_kv) ptx::grid_dependency_wait();
 
-  // New-token rows: CTA b % grid writes request b's row into its page.  A
-  // CTA that streams that page may read it before or after this write, so
-  // every consumer substitutes the row in shared memory (below) instead.
-  if (p.new_rows != nullptr) {
+  // New-token rows: CTA b % grid stores request b's row into its page.  A CTA
+  // of this launch may stream that page before or after the store, so every
+  // consumer substitutes the row in shared memory instead of reading it from
+  // the pool.  (Storing from the producer warp after its loads measured
+  // slightly slower.)
+  if (p.new_rows != nullptr && warp < kConsumerWarps) {
     for (int b = blockIdx.x; b < p.n_requests; b += p.grid) {
       const int pos = p.positions[b];
       const int lp = pos >= 0 ? pos / kPage : -1;
@@ -283,9 +291,10 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       const uint4* src = reinterpret_cast<const uint4*>(p.new_rows + (size_t)b * p.row_elems);
       uint4* dst = reinterpret_cast<uint4*>(p.pool + ((size_t)page * kPage + pos % kPage) *
                                                          (size_t)p.row_elems);
-      for (int i = threadIdx.x; i < p.row_elems / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+      for (int i = threadIdx.x; i < p.row_elems / 8; i += kConsumers) dst[i] = __ldg(src + i);
     }
   }
+
 
   const long long cta_start = (long long)blockIdx.x * p.total_pages / p.grid;
   const long long cta_end = (long long)(blockIdx.x + 1) * p.total_pages / p.grid;
@@ -313,6 +322,10 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         const int my_pid = lane < cnt ? __ldg(prow + base + lane) : 0;
         for (int j = 0; j < cnt; ++j) {
           const int pid = __shfl_sync(0xffffffffu, my_pid, j);
+          // Early loads only fill the ring: the producer waits for earlier
+          // kernels before its first (bounded) wait on a consumer release,
+          // which would otherwise count the consumers' own dependency wait.
+          if (early_kv && it == kStages) ptx::grid_dependency_wait();
           int good = 1;
           if (lane == 0) {
             const int s = it % kStages;
@@ -398,10 +411,13 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     int poisoned = 0;
     // The new token of this request, if it falls in this segment's pages:
     // its K slice (chunk `lane`) and V slice (chunk `lane`) of kv head g.
+    // The position's load is issued before the Q loads below and the row's
+    // loads are consumed only at the substitution, so neither adds a round
+    // trip to the segment's start.
+    const int pos = p.new_rows != nullptr ? __ldg(p.positions + b) : -1;
     int sub_pos = -1;
     uint4 sub_k = make_uint4(0u, 0u, 0u, 0u), sub_v = make_uint4(0u, 0u, 0u, 0u);
-    if (p.new_rows != nullptr) {
-      const int pos = p.positions[b];
+    auto load_new_row = [&]() {
       if (pos >= max(U.tok_start, first_page_tok + lo * kPage) &&
           pos < min(U.tok_end, first_page_tok + hi * kPage)) {
         sub_pos = pos;
@@ -409,7 +425,7 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         sub_k = __ldg(row + (g * kD) / 8 + lane);
         sub_v = __ldg(row + ((Hkv + g) * kD) / 8 + lane);
       }
-    }
+    };
 
     float* xo_g = sh.xo + (tg * kMaxG) * kXRow;   // this token group's exchange rows
     float* xml_g = sh.xml + (tg * kMaxG) * 2;
@@ -431,6 +447,7 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
           qfrag[kk * 32 + lane] = v;
         }
       }
+      load_new_row();
       ptx::named_barrier(1, kConsumers);
       MmaState st;
 #pragma unroll
@@ -596,6 +613,7 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       }
     } else {
       // ---------------- CUDA-core variant ----------------
+      load_new_row();
       FmaState st;
       float qf[kMaxG][8];
 #pragma unroll
@@ -763,9 +781,11 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     }
     if (!single) {
       // The last CTA to finish this unit merges every partial, in CTA order.
-      __threadfence();
+      // The barrier orders every thread's partial before thread 0's fence,
+      // which publishes them all at device scope before the count.
       ptx::named_barrier(1, kConsumers);
       if (ct == 0) {
+        __threadfence();
         const int prev = atomicAdd(p.counters + u, 1);
         *sh.merge_flag = (prev == U.n_parts - 1) ? 1 : 0;
       }
@@ -820,7 +840,8 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         }
         ptx::named_barrier(1, kConsumers);
         // Each thread owns up to two float4 outputs and issues the loads of
-        // both (kBatch partials each) before any arithmetic.
+        // both (kBatch partials each) before any arithmetic.  (Issuing the
+        // first batch before the statistics above measured 4% slower.)
         constexpr int kVec = kD / 4;        // float4 per output row
         constexpr int kBatch = kTensorCores ? 12 : 6;  // register headroom differs
         constexpr size_t kPartStride = (size_t)kMaxG * kVec;
@@ -962,7 +983,8 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
         const int32_t* page_table, int max_pages, const int32_t* tiles, int B, int T,
         int n_q_heads, int n_kv_heads, int head_dim, float scale, float* out, float* lse,
         void* workspace, size_t ws_bytes, cudaStream_t stream,
-        const int32_t* positions = nullptr, const void* new_rows = nullptr) {
+        const int32_t* positions = nullptr, const void* new_rows = nullptr,
+        unsigned flags = 0) {
   clear_error();
   PA_REQUIRE(B >= 0 && T >= 0, "B and T must be >= 0 (got %d, %d)", B, T);
   if ((long long)B * T == 0) return PA_OK;
@@ -994,6 +1016,7 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
                "tile %lld of request %lld is [%d, %d), outside [0, %lld]", i % T, i / T, s, e,
                max_tok);
   }
+  PA_REQUIRE((flags & ~PA_DECODE_KV_READY) == 0, "unknown flags %#x", flags);
   PA_REQUIRE((positions == nullptr) == (new_rows == nullptr),
              "positions and new_rows go together");
   PA_REQUIRE(new_rows == nullptr || reinterpret_cast<uintptr_t>(new_rows) % 16 == 0,
@@ -1052,6 +1075,7 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
   common.new_rows = static_cast<const __nv_bfloat16*>(new_rows);
   common.positions = positions;
   common.row_elems = row_elems;
+  common.kv_ready = (flags & PA_DECODE_KV_READY) ? 1 : 0;
 
   // Launches of at most kMaxUnitsLarge units each; every launch partitions its
   // own pages and reuses the workspace after the previous one (same stream).
@@ -1129,13 +1153,14 @@ extern "C" int paged_decode_attn_lse_append(const void* q, void* pool, int64_t p
                                             int n_kv_heads, int head_dim, float scale,
                                             const int32_t* positions, const void* new_rows,
                                             float* out, float* lse, void* workspace,
-                                            size_t workspace_bytes, cudaStream_t stream) {
+                                            size_t workspace_bytes, unsigned flags,
+                                            cudaStream_t stream) {
   pa::clear_error();
   if (!positions || !new_rows)
     return pa::fail(PA_ERR_INVALID, "positions and new_rows are required");
   return pa::decode::run(true, q, pool, pool_pages, page_table, max_pages, tiles, B, T,
                          n_q_heads, n_kv_heads, head_dim, scale, out, lse, workspace,
-                         workspace_bytes, stream, positions, new_rows);
+                         workspace_bytes, stream, positions, new_rows, flags);
 }
 
 extern "C" int paged_decode_attn_lse_cuda_core(const void* q, const void* pool,

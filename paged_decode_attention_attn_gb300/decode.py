@@ -26,19 +26,25 @@ from .workloads import DecodeWorkload, history_rows
 
 
 def _layer_kernels(fused, cuda_core, q, pool, table, positions, new_row, tiles, scale, tile_out,
-                   tile_lse, workspace, status, part_offsets, out, lse, stream):
+                   tile_lse, workspace, status, part_offsets, out, lse, stream, kv_ready=False):
     """The layer's kernels: tail write + attention (one fused launch, or two),
     then the merge of the tiles."""
     geo_h, geo_d = tile_out.shape[-2], tile_out.shape[-1]
+    n_tiles = np.asarray(tiles).shape[1]
     if fused and not cuda_core:
         B.paged_decode_attn_lse_append(q, pool, table, tiles, scale, positions, new_row,
-                                       tile_out, tile_lse, workspace, stream=stream)
+                                       tile_out, tile_lse, workspace, stream=stream,
+                                       kv_ready=kv_ready)
     else:
         B.kv_append_rows(pool, table, positions, new_row, status=status, stream=stream)
         B.paged_decode_attn_lse(q, pool, table, tiles, scale, tile_out, tile_lse, workspace,
                                 stream=stream, cuda_core=cuda_core)
-    B.lse_merge(tile_out.view(-1, geo_h, geo_d), tile_lse.view(-1, geo_h), part_offsets, out,
-                lse, stream=stream)
+    if n_tiles > 1:
+        # With one tile per request the merge is the identity (a single
+        # partial is returned bit for bit): out and lse are views of the tile
+        # outputs and no merge launch is needed.
+        B.lse_merge(tile_out.view(-1, geo_h, geo_d), tile_lse.view(-1, geo_h), part_offsets,
+                    out, lse, stream=stream)
 
 
 class _Outputs:
@@ -48,10 +54,14 @@ class _Outputs:
                                     dtype=torch.float32, device=device)
         self.tile_lse = torch.empty((n_layers, w.batch, w.n_tiles, geo.n_q_heads),
                                     dtype=torch.float32, device=device)
-        self.out = torch.empty((n_layers, w.batch, geo.n_q_heads, geo.head_dim),
-                               dtype=torch.float32, device=device)
-        self.lse = torch.empty((n_layers, w.batch, geo.n_q_heads), dtype=torch.float32,
-                               device=device)
+        if w.n_tiles == 1:
+            self.out = self.tile_out[:, :, 0]
+            self.lse = self.tile_lse[:, :, 0]
+        else:
+            self.out = torch.empty((n_layers, w.batch, geo.n_q_heads, geo.head_dim),
+                                   dtype=torch.float32, device=device)
+            self.lse = torch.empty((n_layers, w.batch, geo.n_q_heads), dtype=torch.float32,
+                                   device=device)
         self.part_offsets = torch.arange(0, (w.batch + 1) * w.n_tiles, w.n_tiles,
                                          dtype=torch.int32, device=device)
 
@@ -60,11 +70,18 @@ class ResidentDecode:
     """Decode step over a device-resident pool [layers][pages][64][row_elems]."""
 
     def __init__(self, w: DecodeWorkload, t: dict, cuda_core: bool = False,
-                 tiles: np.ndarray | None = None, stream=None, fused: bool = True):
+                 tiles: np.ndarray | None = None, stream=None, fused: bool = True,
+                 kv_ready: bool = False):
         self.w = w
         self.t = t
         self.cuda_core = cuda_core
         self.fused = fused
+        # The pool and page table change only through this object's own
+        # launches (each layer's new row, stored by that layer's launch), so
+        # the caller may let each launch load pages before the previous
+        # kernel ends; it must then not write them with other kernels
+        # between steps without a stream synchronisation.
+        self.kv_ready = kv_ready
         self.tiles = np.ascontiguousarray(w.tiles if tiles is None else tiles, dtype=np.int32)
         self.n_layers = t["pool"].shape[0]
         dev = t["pool"].device
@@ -89,7 +106,7 @@ class ResidentDecode:
         _layer_kernels(self.fused, self.cuda_core, t["q"][i], t["pool"][i], t["page_table"],
                        t["positions"], t["new_rows"][i], self.tiles, geo.scale, o.tile_out[i],
                        o.tile_lse[i], self.workspace, self.status, o.part_offsets, o.out[i],
-                       o.lse[i], self.stream)
+                       o.lse[i], self.stream, kv_ready=self.kv_ready)
 
     def step(self):
         for i in range(self.n_layers):
@@ -328,14 +345,12 @@ class PlannedDecode:
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.workspace = B.alloc_workspace(w.batch, 1, geo.n_q_heads, geo.n_kv_heads,
                                            geo.head_dim, device=dev)
-        self.out = torch.empty((self.n_layers, w.batch, geo.n_q_heads, geo.head_dim),
-                               dtype=torch.float32, device=dev)
-        self.lse = torch.empty((self.n_layers, w.batch, geo.n_q_heads), dtype=torch.float32,
-                               device=dev)
         self.tile_out = torch.empty((self.n_layers, w.batch, 1, geo.n_q_heads, geo.head_dim),
                                     dtype=torch.float32, device=dev)
         self.tile_lse = torch.empty((self.n_layers, w.batch, 1, geo.n_q_heads),
                                     dtype=torch.float32, device=dev)
+        self.out = self.tile_out[:, :, 0]        # one tile per request: no merge
+        self.lse = self.tile_lse[:, :, 0]
         self.part_offsets = torch.arange(0, w.batch + 1, dtype=torch.int32, device=dev)
         self.resident = [dict() for _ in range(w.batch)]
 

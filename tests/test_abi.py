@@ -96,11 +96,13 @@ def test_fused_append_argument_checks(B):
     fake = 1 << 20
     arr = np.ascontiguousarray(np.asarray([[[0, 64]]], dtype=np.int32))
 
-    def call(positions, rows):
+    def call(positions, rows, flags=0):
         return B.lib.paged_decode_attn_lse_append(fake, fake, 16, fake, 8, arr.ctypes.data, 1, 1,
                                                   24, 4, 256, 0.0625, positions, rows, fake, fake,
-                                                  fake, 1 << 30, None)
+                                                  fake, 1 << 30, flags, None)
     assert call(None, fake) == B.PA_ERR_INVALID
     assert call(fake, None) == B.PA_ERR_INVALID
     assert call(fake, fake + 8) == B.PA_ERR_INVALID
     assert "new_rows" in B.last_error()
+    assert call(fake, fake, flags=2) == B.PA_ERR_INVALID
+    assert "flags" in B.last_error()

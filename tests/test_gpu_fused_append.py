@@ -127,3 +127,25 @@ def test_fused_bad_position_is_reported_and_not_stored(D):
     changed = (t["pool"].view(torch.int16) != before.view(torch.int16)).any(dim=-1)
     assert changed.nonzero().tolist() == [[0, page, 199 % 64]]    # request 1's row only
     assert torch.isfinite(dec.o.out).all()
+
+
+@pytest.mark.parametrize("make", [edge_workload, lambda: wl.four_requests_31744(n_layers=3)],
+                         ids=["edge", "4x31744"])
+def test_early_page_loads_change_no_bits(D, make):
+    # PA_DECODE_KV_READY lets each launch load its first pages while the
+    # previous kernel (the previous layer's merge) finishes; two steps back
+    # to back must give the same bits as launches that wait first.
+    w = make()
+    t = wl.materialize(w, "cuda")
+    runs = []
+    for kv_ready in (True, False):
+        tc = clone(t)
+        dec = D.ResidentDecode(w, tc, kv_ready=kv_ready)
+        torch.cuda.synchronize()     # the clone's kernels are complete
+        dec.step()
+        dec.step()
+        torch.cuda.synchronize()
+        assert dec.kernel_status() == 0
+        runs.append((dec, tc))
+    (a, ta), (b, tb) = runs
+    assert_same(a, b, ta, tb)
