@@ -6,9 +6,11 @@ TEST INFRASTRUCTURE ONLY.  This package is imported by ``tests/``, by
 package, its C-ABI library or its kernels) may import, call or link it, and it
 imports nothing from that package.
 
-Everything is plain NumPy in float64.  Parity of every function here is pinned
-by the ``-m "not gpu"`` tests in ``tests/test_oracle_pins.py`` (brute force,
-closed forms, invariants and a library second opinion); no function is
+Everything is plain NumPy in float64 (the compact-page format's own steps in
+binary32, as the format defines them).  Parity of every function here is
+pinned by the ``-m "not gpu"`` tests in ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_compact_pins.py`` (brute force, closed forms, invariants,
+a published check value and library second opinions); no function is
 "parity unpinned".
 """
 
@@ -22,3 +24,4 @@ from .paged_attention import (  # noqa: F401
     merge_stress_partials,
     softmax_union,
 )
+from . import compact_pages  # noqa: F401,E402
