@@ -70,6 +70,8 @@ extern "C" {
 #define PA_ERR_OWNER        -5  /* write-back owner differs from the staged owner */
 #define PA_ERR_UNSUPPORTED  -6  /* geometry not built into this library */
 #define PA_ERR_REFUSED      -7  /* admission refused (the caller queues the request) */
+#define PA_ERR_TIMEOUT      -8  /* a bounded host wait gave up */
+#define PA_ERR_CRC          -9  /* a compact page does not match its published CRC */
 
 /* Bits OR-ed into the int32 status word at byte 0 of the decode workspace
  * (and of the optional status word of kv_append_rows) by device code. */
@@ -512,6 +514,107 @@ int kv_planner_resident(const kv_planner* planner, uint64_t ctx, int32_t* logica
 int kv_planner_copied(const kv_planner* planner, uint64_t ctx, int32_t* logical, int cap,
                       int* n_out);
 int kv_planner_get_counters(const kv_planner* planner, kv_planner_counters* out);
+
+/* ------------------------------------------------------------------------ */
+/* Compact older pages  ([KVE-exact], [KVE-tier])                           */
+/* ------------------------------------------------------------------------ */
+
+/* A history page that is fully written in every layer gets a second, smaller
+ * representation, converted by background threads, checked by a CRC and
+ * published; until it is published the page is served exact.  The source
+ * pages name no format; this library's reading, per layer and page:
+ *   - per token row and per (K or V, kv head) slice x of head_dim bf16 values:
+ *     s = max|x| / 127 (binary32), codes c = clamp(round_half_even(x / s),
+ *     -127, 127) as int8 (x / s a binary32 division; s = 0 gives zero codes);
+ *     a page holding a non-finite value is not convertible and stays exact;
+ *   - the page's bytes: codes int8 [64][2*Hkv*D], then scales float32
+ *     little-endian [64][2*Hkv] (133,120 bytes at 4 x 256 instead of 262,144);
+ *   - it stands for the values bf16_rne(binary32(c) * s);
+ *   - its CRC is CRC-32 (reflected polynomial 0xEDB88320, initial value and
+ *     final xor 0xFFFFFFFF) of those bytes. */
+#define PA_COMPACT_CODE_MAX 127
+
+/* Bytes of one layer's compact page; 0 for an unsupported geometry
+ * (n_kv_heads >= 1 and head_dim a positive multiple of 16 are supported). */
+size_t kv_compact_page_bytes(int n_kv_heads, int head_dim);
+
+/* CRC-32 as above of `bytes` bytes, continuing `crc` (0 to start). */
+uint32_t kv_crc32(const void* data, size_t bytes, uint32_t crc);
+
+/* Convert one layer's page synchronously.  rows: host bf16 [64][2*Hkv*D];
+ * out: host buffer of kv_compact_page_bytes bytes; crc (optional) receives
+ * its CRC.  PA_ERR_INVALID if a value is not finite (out then unspecified). */
+int kv_compact_convert_page(const void* rows, int n_kv_heads, int head_dim,
+                            void* out, uint32_t* crc);
+
+typedef struct kv_compactor kv_compactor;
+
+typedef struct {
+    int32_t n_layers;
+    int32_t n_requests;
+    int32_t n_kv_heads;
+    int32_t head_dim;
+    int32_t max_pages;        /* logical pages per request                      */
+    int32_t n_threads;        /* background converter threads, 1..256           */
+    const void* const* exact_rows;   /* [n_layers * n_requests]: host address of
+                                        token 0 of (layer l, request r) at index
+                                        l * n_requests + r; rows are contiguous
+                                        in token order, 4*Hkv*D bytes each      */
+    void* const* compact_pages;      /* [n_layers * n_requests]: host address of
+                                        compact page 0 of (l, r); page p starts
+                                        p * kv_compact_page_bytes later          */
+} kv_compactor_desc;
+
+/* Page states. */
+#define PA_PAGE_EXACT            0  /* not known to be fully written: exact     */
+#define PA_PAGE_QUEUED           1  /* fully written, waiting for a converter   */
+#define PA_PAGE_PUBLISHED        2  /* compact form and CRCs of every layer ready */
+#define PA_PAGE_NOT_CONVERTIBLE  3  /* a non-finite value: stays exact          */
+
+typedef struct {
+    uint64_t published_pages;
+    uint64_t not_convertible_pages;
+    uint64_t compact_bytes;    /* bytes of compact pages written, all layers   */
+    uint64_t queued_pages;     /* queued or being converted                    */
+} kv_compactor_counters;
+
+/* Start the converter threads.  All memory (exact history and compact store)
+ * is the caller's and must outlive the compactor; the two address arrays are
+ * copied. */
+int kv_compactor_create(const kv_compactor_desc* desc, kv_compactor** out);
+
+/* Stop the threads; a page being converted is finished first (the call waits
+ * for it, milliseconds).  Queued pages are dropped. */
+int kv_compactor_destroy(kv_compactor* c);
+
+/* The caller states that pages [0, full_pages) of `request` are fully written
+ * in every layer, in host memory (the write-backs that wrote them have
+ * completed).  Pages not yet known are queued for conversion; the rest are
+ * left as they are.  Never blocks on a conversion. */
+int kv_compactor_mark_written(kv_compactor* c, int request, int full_pages);
+
+/* hold != 0: converters start no new page (queued pages stay queued, served
+ * exact); hold == 0: resume. */
+int kv_compactor_hold(kv_compactor* c, int hold);
+
+/* Wait until no page is queued or being converted.  PA_ERR_TIMEOUT after
+ * timeout_ms; PA_ERR_ORDER if the converter is held with pages queued. */
+int kv_compactor_wait_idle(kv_compactor* c, int timeout_ms);
+
+/* States (PA_PAGE_*) of pages [first_page, first_page + n_pages) of a
+ * request.  A page read as PA_PAGE_PUBLISHED has its compact bytes and CRCs
+ * visible to this thread. */
+int kv_compactor_states(const kv_compactor* c, int request, int first_page, int n_pages,
+                        uint8_t* states);
+
+/* The published CRC of (layer, request, page); PA_ERR_ORDER if unpublished. */
+int kv_compactor_crc(const kv_compactor* c, int layer, int request, int page, uint32_t* crc);
+
+/* Recompute every layer's CRC of a published page and compare with the
+ * published ones: PA_OK or PA_ERR_CRC. */
+int kv_compactor_verify(const kv_compactor* c, int request, int page);
+
+int kv_compactor_get_counters(const kv_compactor* c, kv_compactor_counters* out);
 
 #ifdef __cplusplus
 }

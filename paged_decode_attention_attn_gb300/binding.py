@@ -24,10 +24,13 @@ PA_ERR_ORDER = -4
 PA_ERR_OWNER = -5
 PA_ERR_UNSUPPORTED = -6
 PA_ERR_REFUSED = -7
+PA_ERR_TIMEOUT = -8
+PA_ERR_CRC = -9
 PA_STATUS_BAD_PAGE = 1
 PA_STATUS_TIMEOUT = 2
 PA_STATUS_BAD_ROW = 4
 PA_ARENA_RECORD_ONLY = 1
+PA_PAGE_EXACT, PA_PAGE_QUEUED, PA_PAGE_PUBLISHED, PA_PAGE_NOT_CONVERTIBLE = 0, 1, 2, 3
 PA_DECODE_KV_READY = 1
 PAGE_TOKENS = 64
 
@@ -46,6 +49,10 @@ EXPORTED = [
     "kv_planner_create", "kv_planner_destroy", "kv_planner_info", "kv_planner_admit",
     "kv_planner_set_target", "kv_planner_release", "kv_planner_step", "kv_planner_resident",
     "kv_planner_copied", "kv_planner_get_counters",
+    "kv_compact_page_bytes", "kv_crc32", "kv_compact_convert_page", "kv_compactor_create",
+    "kv_compactor_destroy", "kv_compactor_mark_written", "kv_compactor_hold",
+    "kv_compactor_wait_idle", "kv_compactor_states", "kv_compactor_crc", "kv_compactor_verify",
+    "kv_compactor_get_counters",
 ]
 
 
@@ -134,6 +141,27 @@ class KvReceipt(ctypes.Structure):
         ("tickets_released", ctypes.c_int32),
         ("pad_", ctypes.c_int32),
     ]
+
+
+class KvCompactorDesc(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32),
+        ("n_requests", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("max_pages", ctypes.c_int32),
+        ("n_threads", ctypes.c_int32),
+        ("exact_rows", ctypes.POINTER(ctypes.c_void_p)),
+        ("compact_pages", ctypes.POINTER(ctypes.c_void_p)),
+    ]
+
+
+class KvCompactorCounters(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in (
+        "published_pages", "not_convertible_pages", "compact_bytes", "queued_pages")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class KvPlannerDesc(ctypes.Structure):
@@ -248,6 +276,31 @@ def _load():
     lib.kv_planner_copied.argtypes = [vp, ctypes.c_uint64, i32p, i32, ctypes.POINTER(ctypes.c_int)]
     lib.kv_planner_get_counters.restype = i32
     lib.kv_planner_get_counters.argtypes = [vp, ctypes.POINTER(KvPlannerCounters)]
+    u32 = ctypes.c_uint32
+    lib.kv_compact_page_bytes.restype = sz
+    lib.kv_compact_page_bytes.argtypes = [i32, i32]
+    lib.kv_crc32.restype = u32
+    lib.kv_crc32.argtypes = [vp, sz, u32]
+    lib.kv_compact_convert_page.restype = i32
+    lib.kv_compact_convert_page.argtypes = [vp, i32, i32, vp, ctypes.POINTER(u32)]
+    lib.kv_compactor_create.restype = i32
+    lib.kv_compactor_create.argtypes = [ctypes.POINTER(KvCompactorDesc), ctypes.POINTER(vp)]
+    lib.kv_compactor_destroy.restype = i32
+    lib.kv_compactor_destroy.argtypes = [vp]
+    lib.kv_compactor_mark_written.restype = i32
+    lib.kv_compactor_mark_written.argtypes = [vp, i32, i32]
+    lib.kv_compactor_hold.restype = i32
+    lib.kv_compactor_hold.argtypes = [vp, i32]
+    lib.kv_compactor_wait_idle.restype = i32
+    lib.kv_compactor_wait_idle.argtypes = [vp, i32]
+    lib.kv_compactor_states.restype = i32
+    lib.kv_compactor_states.argtypes = [vp, i32, i32, i32, ctypes.POINTER(ctypes.c_uint8)]
+    lib.kv_compactor_crc.restype = i32
+    lib.kv_compactor_crc.argtypes = [vp, i32, i32, i32, ctypes.POINTER(u32)]
+    lib.kv_compactor_verify.restype = i32
+    lib.kv_compactor_verify.argtypes = [vp, i32, i32]
+    lib.kv_compactor_get_counters.restype = i32
+    lib.kv_compactor_get_counters.argtypes = [vp, ctypes.POINTER(KvCompactorCounters)]
     return lib
 
 
@@ -639,6 +692,96 @@ class Planner:
     def close(self):
         if self.handle:
             lib.kv_planner_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+# ---------------------------------------------------------------------------
+# Compact older pages
+# ---------------------------------------------------------------------------
+
+def compact_page_bytes(n_kv_heads: int, head_dim: int) -> int:
+    return int(lib.kv_compact_page_bytes(n_kv_heads, head_dim))
+
+
+def crc32(data: bytes, crc: int = 0) -> int:
+    buf = ctypes.create_string_buffer(bytes(data), len(data))
+    return int(lib.kv_crc32(buf, len(data), crc))
+
+
+def compact_convert_page(rows, n_kv_heads: int, head_dim: int):
+    """rows: host bf16 tensor [64][2*Hkv*D].  Returns (page bytes, crc)."""
+    if rows.device.type != "cpu" or rows.dtype != torch.bfloat16 or not rows.is_contiguous():
+        raise ValueError("rows must be a contiguous CPU bf16 tensor")
+    n = compact_page_bytes(n_kv_heads, head_dim)
+    out = ctypes.create_string_buffer(n)
+    crc = ctypes.c_uint32()
+    _check(lib.kv_compact_convert_page(rows.data_ptr(), n_kv_heads, head_dim, out,
+                                       ctypes.byref(crc)))
+    return out.raw, crc.value
+
+
+class Compactor:
+    """Background converter of fully written pages into their compact form.
+
+    exact_rows / compact_pages: host addresses, index layer * n_requests +
+    request (see kv_compactor_desc)."""
+
+    def __init__(self, n_layers, n_requests, n_kv_heads, head_dim, max_pages, exact_rows,
+                 compact_pages, n_threads=4):
+        n = n_layers * n_requests
+        if len(exact_rows) != n or len(compact_pages) != n:
+            raise ValueError("one exact and one compact address per (layer, request)")
+        self._exact = (ctypes.c_void_p * n)(*exact_rows)
+        self._compact = (ctypes.c_void_p * n)(*compact_pages)
+        d = KvCompactorDesc()
+        d.n_layers, d.n_requests, d.n_kv_heads, d.head_dim = (n_layers, n_requests, n_kv_heads,
+                                                              head_dim)
+        d.max_pages, d.n_threads = max_pages, n_threads
+        d.exact_rows = ctypes.cast(self._exact, ctypes.POINTER(ctypes.c_void_p))
+        d.compact_pages = ctypes.cast(self._compact, ctypes.POINTER(ctypes.c_void_p))
+        h = ctypes.c_void_p()
+        _check(lib.kv_compactor_create(ctypes.byref(d), ctypes.byref(h)))
+        self.handle = h
+        self.max_pages = max_pages
+        self.n_layers = n_layers
+
+    def mark_written(self, request: int, full_pages: int):
+        _check(lib.kv_compactor_mark_written(self.handle, request, full_pages))
+
+    def hold(self, on: bool):
+        _check(lib.kv_compactor_hold(self.handle, 1 if on else 0))
+
+    def wait_idle(self, timeout_ms: int = 600000):
+        _check(lib.kv_compactor_wait_idle(self.handle, timeout_ms))
+
+    def states(self, request: int, first_page: int = 0, n_pages=None):
+        n = self.max_pages - first_page if n_pages is None else n_pages
+        arr = (ctypes.c_uint8 * max(1, n))()
+        _check(lib.kv_compactor_states(self.handle, request, first_page, n, arr))
+        return list(arr[:n])
+
+    def crc(self, layer: int, request: int, page: int) -> int:
+        c = ctypes.c_uint32()
+        _check(lib.kv_compactor_crc(self.handle, layer, request, page, ctypes.byref(c)))
+        return c.value
+
+    def verify(self, request: int, page: int):
+        _check(lib.kv_compactor_verify(self.handle, request, page))
+
+    def counters(self) -> dict:
+        c = KvCompactorCounters()
+        _check(lib.kv_compactor_get_counters(self.handle, ctypes.byref(c)))
+        return c.as_dict()
+
+    def close(self):
+        if getattr(self, "handle", None):
+            lib.kv_compactor_destroy(self.handle)
             self.handle = None
 
     def __del__(self):
