@@ -267,6 +267,14 @@ typedef struct {
     cudaStream_t h2d_stream;      /* history copies                                */
     cudaStream_t d2h_stream;      /* tail write-back                               */
     uint32_t     flags;           /* PA_ARENA_* */
+    /* Compact runs ([KVE-exact] "runs of two representations"; optional): a
+     * staged compact page lands in the slot's landing area and is expanded on
+     * the H2D stream into a full bf16 page of the slot.  0 / 0 / 0: refused. */
+    int32_t      compact_head_dim;  /* head_dim of the compact format            */
+    uint64_t     landing_offset;    /* bytes from device_base to slot 0's landing
+                                       area (256-B aligned, after every page)    */
+    uint64_t     landing_bytes;     /* landing bytes per slot; slot s's area
+                                       starts s * landing_bytes later            */
 } kv_arena_desc;
 
 /* A run of consecutive logical pages of one request.  host_rows != NULL: a
@@ -277,8 +285,11 @@ typedef struct {
     int32_t     logical_page;
     int32_t     n_pages;
     int64_t     n_rows;
-    const void* host_rows;
-    int64_t     resident_page;
+    const void* host_rows;      /* exact run: pinned host rows, n_rows of them  */
+    int64_t     resident_page;  /* resident run (host_rows and host_compact NULL) */
+    const void* host_compact;   /* compact run: pinned host compact pages (n_pages
+                                   of kv_compact_page_bytes each, consecutive);
+                                   n_rows must be n_pages * 64 (fully written)   */
 } kv_page_run;
 
 typedef struct {
@@ -324,9 +335,13 @@ int kv_arena_drain(kv_arena* arena);
 /* Stage one layer: picks the next slot (round robin), makes the H2D stream
  * wait on that slot's previous attention and write-back events, enqueues one
  * H2D copy per staged run, writes the slot's page-table rows for every run
- * (staged runs get consecutive slot pages in request/run order), records the
- * slot's copy event and makes the compute stream wait on it.  PA_ERR_ORDER if
- * the slot's previous stage was never marked attention-done.
+ * (staged runs, exact or compact, get consecutive slot pages in request/run
+ * order), records the slot's copy event and makes the compute stream wait on
+ * it.  A compact run is copied into the slot's landing area and expanded, on
+ * the H2D stream before the copy event, into bf16 pages holding
+ * bf16_rne(c * s) (the values the compact page stands for); the attention then
+ * reads it like any page.  PA_ERR_ORDER if the slot's previous stage was never
+ * marked attention-done.
  *   *slot_out        the slot used; *page_table_out its device page table
  *                    ([max_requests][max_pages]) to pass to the attention. */
 int kv_stage_layer(kv_arena* arena, int layer, const kv_stage_req* reqs,

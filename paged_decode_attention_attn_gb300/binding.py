@@ -78,6 +78,9 @@ class KvArenaDesc(ctypes.Structure):
         ("h2d_stream", ctypes.c_void_p),
         ("d2h_stream", ctypes.c_void_p),
         ("flags", ctypes.c_uint32),
+        ("compact_head_dim", ctypes.c_int32),
+        ("landing_offset", ctypes.c_uint64),
+        ("landing_bytes", ctypes.c_uint64),
     ]
 
 
@@ -88,6 +91,7 @@ class KvPageRun(ctypes.Structure):
         ("n_rows", ctypes.c_int64),
         ("host_rows", ctypes.c_void_p),
         ("resident_page", ctypes.c_int64),
+        ("host_compact", ctypes.c_void_p),
     ]
 
 
@@ -456,7 +460,8 @@ class Arena:
     def __init__(self, device_base: int, device_bytes: int, row_bytes: int, n_slots: int,
                  slot_first_page: int, slot_pages: int, page_tables: int, max_requests: int,
                  max_pages: int, compute_stream=None, h2d_stream=None, d2h_stream=None,
-                 record_only: bool = False):
+                 record_only: bool = False, compact_head_dim: int = 0, landing_offset: int = 0,
+                 landing_bytes: int = 0):
         d = KvArenaDesc()
         d.device_base = device_base
         d.device_bytes = device_bytes
@@ -472,6 +477,9 @@ class Arena:
         d.h2d_stream = self._h(h2d_stream)
         d.d2h_stream = self._h(d2h_stream)
         d.flags = PA_ARENA_RECORD_ONLY if record_only else 0
+        d.compact_head_dim = compact_head_dim
+        d.landing_offset = landing_offset
+        d.landing_bytes = landing_bytes
         self._desc = d
         h = ctypes.c_void_p()
         _check(lib.kv_arena_create(ctypes.byref(d), ctypes.byref(h)))
@@ -488,7 +496,8 @@ class Arena:
 
     def stage_layer(self, layer: int, requests):
         """requests: list of (request, owner, [runs]); a run is a dict with
-        logical_page, n_pages and either host_rows (address) + n_rows, or
+        logical_page, n_pages and either host_rows (address) + n_rows,
+        host_compact (address of compact pages) + n_rows = n_pages * 64, or
         resident_page.  Returns (slot, page_table_address)."""
         reqs = (KvStageReq * len(requests))()
         keep = []
@@ -500,6 +509,7 @@ class Arena:
                 arr[k].n_rows = r.get("n_rows", 0)
                 arr[k].host_rows = r.get("host_rows")
                 arr[k].resident_page = r.get("resident_page", 0)
+                arr[k].host_compact = r.get("host_compact")
             keep.append(arr)
             reqs[i].request = request
             reqs[i].n_runs = len(runs)
@@ -536,6 +546,7 @@ class Arena:
                 arr[k].n_rows = r.get("n_rows", 0)
                 arr[k].host_rows = r.get("host_rows")
                 arr[k].resident_page = r.get("resident_page", 0)
+                arr[k].host_compact = r.get("host_compact")
             keep.append(arr)
             reqs[i].request = request
             reqs[i].n_runs = len(runs)

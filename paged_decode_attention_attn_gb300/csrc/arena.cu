@@ -28,6 +28,7 @@
 //     exactly those events, and retired with host waits that produce a receipt.
 //     Copy tickets pin the generation of the host pages a lease copies from, so
 //     those pages cannot be recycled while a copy may still read them.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cinttypes>
@@ -66,6 +67,68 @@ __global__ void fill_page_table_kernel(const __grid_constant__ TableParams p) {
     int32_t* row = p.table + (size_t)run.request * p.max_pages + run.logical_page;
     for (int i = threadIdx.x; i < run.n_pages; i += blockDim.x)
       row[i] = static_cast<int32_t>(run.first_page + i);
+  }
+}
+
+struct ExpandRun {
+  long long landing_off;  // bytes from the slot's landing area to the run's first compact page
+  long long first_page;   // device page of the run's first page
+  long long row_start;    // rows of the runs before this one in the launch
+  int32_t n_pages;
+  int32_t pad;
+};
+
+struct ExpandParams {
+  const uint8_t* landing;   // the slot's landing area
+  uint8_t* base;            // device_base
+  long long page_bytes;     // bytes of a bf16 page
+  long long cpage_bytes;    // bytes of a compact page
+  long long total_rows;
+  int row_elems;            // 2 * Hkv * head_dim
+  int head_dim;
+  int n_runs;
+  ExpandRun runs[kMaxRunsPerLaunch];
+};
+
+// Rebuilds bf16 rows from compact pages: value = bf16_rne(float(code) * scale)
+// with one binary32 scale per (row, K or V, kv head) slice.  One block per
+// row (grid-stride); each thread turns 16 codes into 16 bf16 values.
+__global__ void expand_compact_kernel(const __grid_constant__ ExpandParams p) {
+  const int chunks = p.row_elems / 16;
+  const int slices = p.row_elems / p.head_dim;
+  for (long long row = blockIdx.x; row < p.total_rows; row += gridDim.x) {
+    int r = 0;
+    while (r + 1 < p.n_runs && p.runs[r + 1].row_start <= row) ++r;
+    const ExpandRun run = p.runs[r];
+    const long long rr = row - run.row_start;
+    const long long page = rr / PA_PAGE_TOKENS;
+    const int t = static_cast<int>(rr - page * PA_PAGE_TOKENS);
+    const uint8_t* cpage = p.landing + run.landing_off + page * p.cpage_bytes;
+    const int8_t* codes = reinterpret_cast<const int8_t*>(cpage) + (size_t)t * p.row_elems;
+    const float* scales = reinterpret_cast<const float*>(
+        cpage + (size_t)PA_PAGE_TOKENS * p.row_elems) + (size_t)t * slices;
+    uint8_t* dst = p.base + (run.first_page + page) * p.page_bytes +
+                   (size_t)t * p.row_elems * 2;
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) {
+      const float s = scales[(c * 16) / p.head_dim];
+      const uint4 raw = *reinterpret_cast<const uint4*>(codes + c * 16);
+      const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+      uint32_t out[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const uint32_t word = w[k / 2];
+        const int sh = (k % 2) * 16;
+        const float lo = static_cast<float>(static_cast<int8_t>((word >> sh) & 0xFFu));
+        const float hi = static_cast<float>(static_cast<int8_t>((word >> (sh + 8)) & 0xFFu));
+        const __nv_bfloat16 blo = __float2bfloat16_rn(__fmul_rn(lo, s));
+        const __nv_bfloat16 bhi = __float2bfloat16_rn(__fmul_rn(hi, s));
+        out[k] = static_cast<uint32_t>(__bfloat16_as_ushort(blo)) |
+                 (static_cast<uint32_t>(__bfloat16_as_ushort(bhi)) << 16);
+      }
+      uint4* d4 = reinterpret_cast<uint4*>(dst + (size_t)c * 32);
+      d4[0] = make_uint4(out[0], out[1], out[2], out[3]);
+      d4[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
   }
 }
 
@@ -135,6 +198,7 @@ struct kv_arena {
   uint64_t slot_reuses = 0;
   int64_t page_bytes = 0;
   int64_t arena_pages = 0;
+  int64_t cpage_bytes = 0;      // compact page bytes (0: no compact runs)
   pa::arena::Mode mode = pa::arena::kModeUnset;
   std::map<uint64_t, pa::arena::Lease> leases;      // begun, not yet retired
   std::map<uint64_t, pa::arena::HostOwner> owners;  // host page generations
@@ -247,12 +311,35 @@ int op_table(kv_arena* a, cudaStream_t s, int slot, const TableParams& p) {
   return e == cudaSuccess ? PA_OK : quarantine(a, "page-table kernel launch", e);
 }
 
+int op_expand(kv_arena* a, cudaStream_t s, int slot, const ExpandParams& p) {
+  if (injected_failure(a)) return quarantine(a, "expand kernel launch", cudaSuccess);
+  if (a->record_only) {
+    std::string line;
+    char buf[96];
+    snprintf(buf, sizeof(buf), "%s expand slot=%d runs=%d", stream_name(a, s), slot, p.n_runs);
+    line = buf;
+    for (int i = 0; i < p.n_runs; ++i) {
+      snprintf(buf, sizeof(buf), " +%lld:%d->%lld", p.runs[i].landing_off, p.runs[i].n_pages,
+               p.runs[i].first_page);
+      line += buf;
+    }
+    a->log += line;
+    a->log += '\n';
+    return PA_OK;
+  }
+  const long long blocks = std::min<long long>(p.total_rows, 8192);
+  expand_compact_kernel<<<(unsigned)(blocks < 1 ? 1 : blocks), 128, 0, s>>>(p);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? PA_OK : quarantine(a, "expand kernel launch", e);
+}
+
 // Checks a stage request list against the arena; submits nothing.
 int validate_stage(kv_arena* a, const kv_stage_req* reqs, int n_reqs) {
   const kv_arena_desc& d = a->d;
   PA_REQUIRE(n_reqs >= 0 && (n_reqs == 0 || reqs), "bad request list");
   std::vector<char> seen(d.max_requests, 0);
   int64_t staged_pages = 0;
+  uint64_t landing_used = 0;
   for (int i = 0; i < n_reqs; ++i) {
     const kv_stage_req& r = reqs[i];
     PA_REQUIRE(r.request >= 0 && r.request < d.max_requests, "request %d outside [0, %d)",
@@ -267,7 +354,22 @@ int validate_stage(kv_arena* a, const kv_stage_req* reqs, int n_reqs) {
                      (int64_t)run.logical_page + run.n_pages <= d.max_pages,
                  "request %d run %d: pages [%d, +%d) outside the table", r.request, k,
                  run.logical_page, run.n_pages);
-      if (run.host_rows) {
+      if (run.host_compact) {
+        PA_REQUIRE(!run.host_rows, "request %d run %d: both exact and compact", r.request, k);
+        PA_REQUIRE(a->cpage_bytes > 0, "request %d run %d: this arena has no landing area",
+                   r.request, k);
+        PA_REQUIRE(run.n_rows == (int64_t)run.n_pages * d.page_tokens,
+                   "request %d run %d: a compact run holds fully written pages only", r.request,
+                   k);
+        if (!a->record_only) {
+          cudaPointerAttributes attr;
+          const cudaError_t e = cudaPointerGetAttributes(&attr, run.host_compact);
+          PA_REQUIRE(e == cudaSuccess && attr.type == cudaMemoryTypeHost,
+                     "request %d run %d: compact pages must be pinned host memory", r.request, k);
+        }
+        landing_used += (uint64_t)run.n_pages * a->cpage_bytes;
+        staged_pages += run.n_pages;
+      } else if (run.host_rows) {
         PA_REQUIRE(run.n_rows >= 0 && run.n_rows <= (int64_t)run.n_pages * d.page_tokens,
                    "request %d run %d: %" PRId64 " rows do not fit %d pages", r.request, k,
                    run.n_rows, run.n_pages);
@@ -286,6 +388,9 @@ int validate_stage(kv_arena* a, const kv_stage_req* reqs, int n_reqs) {
   }
   PA_REQUIRE(staged_pages <= d.slot_pages, "stage needs %" PRId64 " pages, a slot holds %" PRId64,
              staged_pages, d.slot_pages);
+  PA_REQUIRE(landing_used <= d.landing_bytes,
+             "compact runs need %" PRIu64 " landing bytes, a slot has %" PRIu64, landing_used,
+             (uint64_t)d.landing_bytes);
   return PA_OK;
 }
 
@@ -310,7 +415,10 @@ int submit_stage(kv_arena* a, int slot, bool wait_prior_readers, const kv_stage_
   records->reserve(n_reqs);
   bytes->assign(n_reqs, 0);
   std::vector<TableRun> table_runs;
+  std::vector<ExpandRun> expand_runs;
   int64_t cursor = 0;
+  long long landing_cursor = 0;
+  uint8_t* landing = base + d.landing_offset + (uint64_t)slot * d.landing_bytes;
   for (int i = 0; i < n_reqs; ++i) {
     const kv_stage_req& r = reqs[i];
     ReqRecord rec;
@@ -319,7 +427,18 @@ int submit_stage(kv_arena* a, int slot, bool wait_prior_readers, const kv_stage_
     for (int k = 0; k < r.n_runs; ++k) {
       const kv_page_run& run = r.runs[k];
       int64_t first;
-      if (run.host_rows) {
+      if (run.host_compact) {
+        first = slot_page0 + cursor;
+        cursor += run.n_pages;
+        const size_t nb = (size_t)run.n_pages * a->cpage_bytes;
+        if ((rc = op_copy(a, h2d, landing + landing_cursor, run.host_compact, nb,
+                          cudaMemcpyHostToDevice, first, -1)) != PA_OK)
+          return rc;
+        a->staged_bytes += nb;
+        (*bytes)[i] += nb;
+        expand_runs.push_back(ExpandRun{landing_cursor, first, 0, run.n_pages, 0});
+        landing_cursor += (long long)nb;
+      } else if (run.host_rows) {
         first = slot_page0 + cursor;
         cursor += run.n_pages;
         const size_t nb = (size_t)run.n_rows * d.row_bytes;
@@ -338,6 +457,24 @@ int submit_stage(kv_arena* a, int slot, bool wait_prior_readers, const kv_stage_
       table_runs.push_back(TableRun{r.request, run.logical_page, run.n_pages, 0, first});
     }
     records->push_back(std::move(rec));
+  }
+  for (size_t r0 = 0; r0 < expand_runs.size(); r0 += kMaxRunsPerLaunch) {
+    ExpandParams ep{};
+    ep.landing = landing;
+    ep.base = base;
+    ep.page_bytes = a->page_bytes;
+    ep.cpage_bytes = a->cpage_bytes;
+    ep.row_elems = d.row_bytes / 2;
+    ep.head_dim = d.compact_head_dim;
+    ep.n_runs = static_cast<int>(std::min<size_t>(kMaxRunsPerLaunch, expand_runs.size() - r0));
+    long long rows = 0;
+    for (int k = 0; k < ep.n_runs; ++k) {
+      ep.runs[k] = expand_runs[r0 + k];
+      ep.runs[k].row_start = rows;
+      rows += (long long)ep.runs[k].n_pages * d.page_tokens;
+    }
+    ep.total_rows = rows;
+    if ((rc = op_expand(a, h2d, slot, ep)) != PA_OK) return rc;
   }
   int32_t* table = d.page_tables + (size_t)slot * d.max_requests * d.max_pages;
   for (size_t r0 = 0; r0 < table_runs.size(); r0 += kMaxRunsPerLaunch) {
@@ -443,17 +580,41 @@ extern "C" int kv_arena_create(const kv_arena_desc* desc, kv_arena** out) {
   PA_REQUIRE(d.page_tables != nullptr && d.max_requests >= 1 && d.max_pages >= 1,
              "page_tables, max_requests and max_pages are required");
   const int64_t page_bytes = (int64_t)d.row_bytes * d.page_tokens;
-  const int64_t arena_pages = (int64_t)(d.device_bytes / (uint64_t)page_bytes);
+  // Pages end where the landing areas begin (if there are any).
+  const uint64_t page_area = (d.landing_bytes > 0 && d.landing_offset < d.device_bytes)
+                                 ? d.landing_offset : d.device_bytes;
+  const int64_t arena_pages = (int64_t)(page_area / (uint64_t)page_bytes);
   PA_REQUIRE(d.slot_first_page + (int64_t)d.n_slots * d.slot_pages <= arena_pages,
              "slots need %" PRId64 " pages of %" PRId64 " bytes but device_bytes holds %" PRId64,
              d.slot_first_page + (int64_t)d.n_slots * d.slot_pages, page_bytes, arena_pages);
   PA_REQUIRE(arena_pages < (1ll << 31), "arena too large for 32-bit page ids");
+  int64_t cpage_bytes = 0;
+  if (d.landing_bytes > 0 || d.compact_head_dim != 0) {
+    const int64_t row_elems = d.row_bytes / 2;
+    PA_REQUIRE(d.compact_head_dim >= 16 && d.compact_head_dim % 16 == 0 &&
+                   row_elems % (2 * d.compact_head_dim) == 0,
+               "compact_head_dim (%d) must be a multiple of 16 dividing a row's K and V",
+               d.compact_head_dim);
+    cpage_bytes = (int64_t)kv_compact_page_bytes(
+        static_cast<int>(row_elems / (2 * d.compact_head_dim)), d.compact_head_dim);
+    PA_REQUIRE(d.landing_bytes >= (uint64_t)cpage_bytes,
+               "landing_bytes (%" PRIu64 ") holds no compact page of %" PRId64 " bytes",
+               (uint64_t)d.landing_bytes, cpage_bytes);
+    PA_REQUIRE(d.landing_offset % 256 == 0, "landing_offset must be 256-byte aligned");
+    PA_REQUIRE(d.landing_offset >= (uint64_t)((d.slot_first_page + (int64_t)d.n_slots *
+                                                                       d.slot_pages) *
+                                              page_bytes),
+               "the landing areas must follow every page");
+    PA_REQUIRE(d.landing_offset + (uint64_t)d.n_slots * d.landing_bytes <= d.device_bytes,
+               "landing areas end past device_bytes");
+  }
 
   kv_arena* a = new kv_arena;
   a->d = d;
   a->record_only = (d.flags & PA_ARENA_RECORD_ONLY) != 0;
   a->page_bytes = page_bytes;
   a->arena_pages = arena_pages;
+  a->cpage_bytes = cpage_bytes;
   a->slots.resize(d.n_slots);
   a->ev_copy.assign(d.n_slots, nullptr);
   a->ev_attn.assign(d.n_slots, nullptr);

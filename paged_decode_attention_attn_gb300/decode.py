@@ -169,6 +169,66 @@ class HostHistory:
             pass
 
 
+class CompactStore:
+    """Pinned host store of compact pages beside a HostHistory, filled by the
+    library's background converter ("KV-cache engineering", section "Exact
+    recent pages, compact older pages").
+
+    Compact page p of (layer i, request r) sits at ``address(i, r, p)``; a
+    page is staged compact only once the converter has published it.
+    """
+
+    def __init__(self, w: DecodeWorkload, host: HostHistory, n_threads: int = 8):
+        geo = w.geometry
+        self.w, self.host = w, host
+        self.page_bytes = B.compact_page_bytes(geo.n_kv_heads, geo.head_dim)
+        self.n_layers = len(host.layers)
+        self.offsets = {}
+        total = 0
+        for i in range(self.n_layers):
+            for r in range(w.batch):
+                self.offsets[(i, r)] = total
+                total += w.max_pages * self.page_bytes
+        self.buf = torch.empty(total, dtype=torch.uint8)
+        rc = torch.cuda.cudart().cudaHostRegister(self.buf.data_ptr(), total, 0)
+        code = rc.value if hasattr(rc, "value") else int(rc)
+        if code != 0:
+            raise RuntimeError(f"cudaHostRegister of {total} bytes failed ({rc})")
+        self._registered = True
+        exact = [host.row_address(i, r, 0) for i in range(self.n_layers) for r in range(w.batch)]
+        comp = [self.buf.data_ptr() + self.offsets[(i, r)]
+                for i in range(self.n_layers) for r in range(w.batch)]
+        self.compactor = B.Compactor(self.n_layers, w.batch, geo.n_kv_heads, geo.head_dim,
+                                     w.max_pages, exact, comp, n_threads=n_threads)
+
+    def address(self, i: int, r: int, page: int) -> int:
+        return self.buf.data_ptr() + self.offsets[(i, r)] + page * self.page_bytes
+
+    def mark_written(self, lengths):
+        """Pages below each request's new token are fully written in every
+        layer (the rows before L - 1); queue them for conversion."""
+        pt = self.w.geometry.page_tokens
+        for r, L in enumerate(lengths):
+            self.compactor.mark_written(r, max(0, int(L) - 1) // pt)
+
+    def published(self, r: int):
+        return [s == B.PA_PAGE_PUBLISHED for s in self.compactor.states(r)]
+
+    def close(self):
+        if getattr(self, "compactor", None) is not None:
+            self.compactor.close()
+            self.compactor = None
+        if getattr(self, "_registered", False):
+            torch.cuda.cudart().cudaHostUnregister(self.buf.data_ptr())
+            self._registered = False
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
 class StagedDecode:
     """Decode step with host-owned history staged per layer into arena slots.
 
@@ -179,9 +239,11 @@ class StagedDecode:
 
     def __init__(self, w: DecodeWorkload, t: dict, host: HostHistory, n_slots: int = 2,
                  cuda_core: bool = False, compute_stream=None, h2d_stream=None,
-                 d2h_stream=None, leases: bool = False, fused: bool = True):
+                 d2h_stream=None, leases: bool = False, fused: bool = True,
+                 compact: CompactStore | None = None):
         geo = w.geometry
         self.w, self.t, self.host, self.cuda_core = w, t, host, cuda_core
+        self.compact = compact
         self.leases = leases
         self.fused = fused
         self.step_index = 0
@@ -229,8 +291,14 @@ class StagedDecode:
         self.win_pages = win_pages
         self.slot_pages = max(1, staged_max)
         arena_pages = win_pages + n_slots * self.slot_pages
-        self.arena = torch.empty((arena_pages, pt, geo.row_elems), dtype=torch.bfloat16,
-                                 device=dev)
+        page_bytes = pt * geo.row_bytes
+        landing = 0
+        if compact is not None:                 # room for a slot of compact pages
+            landing = -(-self.slot_pages * compact.page_bytes // 256) * 256
+        self.arena_buf = torch.empty(arena_pages * page_bytes + n_slots * landing,
+                                     dtype=torch.uint8, device=dev)
+        self.arena = self.arena_buf[: arena_pages * page_bytes].view(torch.bfloat16).view(
+            arena_pages, pt, geo.row_elems)
         self.arena.fill_(float("nan"))          # canary: unwritten rows read as NaN
         for (i, r), wb in win_base.items():     # resident window copied in once
             n = w.pages_of(r)
@@ -240,10 +308,16 @@ class StagedDecode:
         self.page_tables = torch.zeros((n_slots, w.batch, w.max_pages), dtype=torch.int32,
                                        device=dev)
         torch.cuda.synchronize(dev)
-        self.handle = B.Arena(self.arena.data_ptr(), self.arena.numel() * 2, geo.row_bytes,
+        self.handle = B.Arena(self.arena_buf.data_ptr(), self.arena_buf.numel(), geo.row_bytes,
                               n_slots, win_pages, self.slot_pages, self.page_tables.data_ptr(),
                               w.batch, w.max_pages, compute_stream=self.compute,
-                              h2d_stream=self.h2d, d2h_stream=self.d2h)
+                              h2d_stream=self.h2d, d2h_stream=self.d2h,
+                              compact_head_dim=geo.head_dim if compact is not None else 0,
+                              landing_offset=arena_pages * page_bytes if landing else 0,
+                              landing_bytes=landing)
+        self.exact_plan = self.plan
+        if compact is not None:
+            self.replan()
         self.o = _Outputs(w, self.n_layers, dev)
         self.workspace = B.alloc_workspace(w.batch, w.n_tiles, geo.n_q_heads, geo.n_kv_heads,
                                            geo.head_dim, device=dev)
@@ -253,6 +327,54 @@ class StagedDecode:
             self.tails.append([(r, int(w.lengths[r]) - 1,
                                 host.row_address(i, r, int(w.lengths[r]) - 1), (i << 32) | r)
                                for r in range(w.batch)])
+
+    def replan(self):
+        """Stage every published page of the exact plan's staged runs in its
+        compact form ("runs of two representations"); the rest stays exact."""
+        pt = self.w.geometry.page_tokens
+        published = [self.compact.published(r) for r in range(self.w.batch)]
+        plan = []
+        for i, reqs in enumerate(self.exact_plan):
+            out = []
+            for r, owner, runs in reqs:
+                L = int(self.w.lengths[r])
+                new_runs = []
+                for run in runs:
+                    if "host_rows" not in run:
+                        new_runs.append(run)
+                        continue
+                    lp, end = run["logical_page"], run["logical_page"] + run["n_pages"]
+                    while lp < end:
+                        kind = published[r][lp]
+                        start = lp
+                        while lp < end and published[r][lp] == kind:
+                            lp += 1
+                        n = lp - start
+                        if kind:
+                            new_runs.append(dict(logical_page=start, n_pages=n, n_rows=n * pt,
+                                                 host_compact=self.compact.address(i, r, start)))
+                        else:
+                            rows = min(lp * pt, L - 1) - start * pt
+                            new_runs.append(dict(logical_page=start, n_pages=n,
+                                                 n_rows=max(0, rows),
+                                                 host_rows=self.host.row_address(i, r,
+                                                                                 start * pt)))
+                out.append((r, owner, new_runs))
+            plan.append(out)
+        self.plan = plan
+
+    def staged_bytes_per_step(self) -> int:
+        """Host-to-device bytes the current plan moves per step."""
+        geo = self.w.geometry
+        total = 0
+        for reqs in self.plan:
+            for _, _, runs in reqs:
+                for run in runs:
+                    if "host_compact" in run:
+                        total += run["n_pages"] * self.compact.page_bytes
+                    elif "host_rows" in run:
+                        total += run["n_rows"] * geo.row_bytes
+        return total
 
     def _kernels(self, i: int, table):
         t, o, geo = self.t, self.o, self.w.geometry

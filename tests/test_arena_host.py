@@ -208,3 +208,70 @@ def test_validation(B):
         assert e.value.code == B.PA_ERR_INVALID
     assert a.call_log() == []
     assert a.stats().stage_generation == 0
+
+
+CPAGE = 133120          # compact page bytes at 4 kv heads x 256
+
+
+def compact(lp, n, host):
+    return dict(logical_page=lp, n_pages=n, n_rows=n * PAGE, host_compact=host)
+
+
+def make_compact_arena(B, n_slots=2, slot_pages=8, window_pages=4, landing_pages=4):
+    page_end = (window_pages + n_slots * slot_pages) * PAGE * ROW
+    landing = landing_pages * CPAGE
+    return B.Arena(BASE, page_end + n_slots * landing, ROW, n_slots, window_pages, slot_pages,
+                   TABLES, 4, 16, compute_stream=1, h2d_stream=2, d2h_stream=3,
+                   record_only=True, compact_head_dim=256, landing_offset=page_end,
+                   landing_bytes=landing)
+
+
+def test_compact_runs_land_then_expand_before_the_copy_event(B):
+    a = make_compact_arena(B)
+    a.stage_layer(0, [(0, 7, [compact(0, 3, 0x1000), staged(3, 2, 0x9000, rows=100)]),
+                      (1, 9, [compact(0, 1, 0x5000), resident(1, 1, 2)])])
+    assert a.call_log() == [
+        "h2d copy h2d bytes=399360 page=4 row=-1",
+        "h2d copy h2d bytes=409600 page=7 row=0",
+        "h2d copy h2d bytes=133120 page=9 row=-1",
+        "h2d expand slot=0 runs=2 +0:3->4 +399360:1->9",
+        "h2d table slot=0 runs=4 0:0+3->4 0:3+2->7 1:0+1->9 1:1+1->2",
+        "h2d record copy[0]",
+        "compute wait copy[0]",
+    ]
+    assert a.stats().staged_bytes == 399360 + 409600 + 133120
+    # slot 1's landing area follows slot 0's
+    a.mark_attention_done(0)
+    a.stage_layer(1, [(0, 7, [compact(0, 2, 0x1000)])])
+    assert a.call_log()[-4] == "h2d expand slot=1 runs=1 +0:2->12"
+
+
+def test_compact_runs_are_checked(B):
+    a = make_compact_arena(B, landing_pages=4)
+    with pytest.raises(B.PagedAttnError) as e:                   # landing holds 4 pages
+        a.stage_layer(0, [(0, 7, [compact(0, 5, 0x1000)])])
+    assert e.value.code == B.PA_ERR_INVALID and "landing" in str(e.value)
+    with pytest.raises(B.PagedAttnError) as e:                   # not fully written
+        a.stage_layer(0, [(0, 7, [dict(logical_page=0, n_pages=2, n_rows=100,
+                                       host_compact=0x1000)])])
+    assert "fully written" in str(e.value)
+    with pytest.raises(B.PagedAttnError):
+        a.stage_layer(0, [(0, 7, [dict(logical_page=0, n_pages=1, n_rows=64, host_rows=0x10,
+                                       host_compact=0x1000)])])
+    assert a.call_log() == []
+    plain = make_arena(B)
+    with pytest.raises(B.PagedAttnError) as e:
+        plain.stage_layer(0, [(0, 7, [compact(0, 1, 0x1000)])])
+    assert "landing" in str(e.value)
+
+
+def test_landing_geometry_is_checked(B):
+    with pytest.raises(B.PagedAttnError):          # landing overlaps the pages
+        B.Arena(BASE, 40 * PAGE * ROW, ROW, 2, 4, 8, TABLES, 4, 16, record_only=True,
+                compact_head_dim=256, landing_offset=10 * PAGE * ROW, landing_bytes=CPAGE)
+    with pytest.raises(B.PagedAttnError):          # smaller than one compact page
+        B.Arena(BASE, 40 * PAGE * ROW, ROW, 2, 4, 8, TABLES, 4, 16, record_only=True,
+                compact_head_dim=256, landing_offset=20 * PAGE * ROW, landing_bytes=CPAGE - 16)
+    with pytest.raises(B.PagedAttnError):          # head_dim does not divide the row
+        B.Arena(BASE, 40 * PAGE * ROW, ROW, 2, 4, 8, TABLES, 4, 16, record_only=True,
+                compact_head_dim=96, landing_offset=20 * PAGE * ROW, landing_bytes=CPAGE)
