@@ -62,6 +62,8 @@ def parse_args():
     ap.add_argument("--no-early-kv", action="store_true",
                     help="make each launch wait for the previous kernel before loading pages")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-compact", action="store_true",
+                    help="skip the end-to-end run with published pages staged compact")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-workers", type=int, default=0)
     ap.add_argument("--bus-model", action="store_true",
@@ -398,13 +400,20 @@ def run_ours(args):
     achieved = kv_bytes_layer / (kern_ms / 1e3) / 1e9
 
     # ---- staged route, end to end through host buffers ----
-    e2e = None
+    e2e = e2e_compact = None
     if not args.no_e2e:
         e2e = run_e2e(args, w, t, dev, D, B)
         # whole job: every rank's bytes over the slowest rank's wall time
         secs = max_over_ranks(e2e.pop("_secs"), world)
         e2e["value"] = round(whole_job_gbs(kv_bytes, e2e["steps"], secs * 1e3, world), 2)
         e2e["ms_per_step"] = round(1e3 * secs / e2e["steps"], 3)
+        if not args.no_compact:
+            e2e_compact = run_e2e(args, w, t, dev, D, B, compact=True,
+                                  exact=(res.o.out, res.o.lse))
+            secs = max_over_ranks(e2e_compact.pop("_secs"), world)
+            e2e_compact["value"] = round(whole_job_gbs(kv_bytes, e2e_compact["steps"],
+                                                       secs * 1e3, world), 2)
+            e2e_compact["ms_per_step"] = round(1e3 * secs / e2e_compact["steps"], 3)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -445,6 +454,8 @@ def run_ours(args):
         }
         if e2e is not None:
             line["e2e"] = e2e
+        if e2e_compact is not None:
+            line["e2e_compact"] = e2e_compact
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -453,13 +464,26 @@ def run_ours(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, w, t, dev, D, B):
-    """Staged route: host-owned history, host Q / new rows in, outputs out."""
+def run_e2e(args, w, t, dev, D, B, compact=False, exact=None):
+    """Staged route: host-owned history, host Q / new rows in, outputs out.
+
+    compact=True: every page below the new token is first converted by the
+    background compactor and staged in its compact form once published
+    ("runs of two representations"); ``exact`` = (out, lse) of the exact
+    route, to report how far the compact form moves the result."""
     import torch
     geo = w.geometry
     host = D.HostHistory(w, t)
     compute = torch.cuda.current_stream(dev)
-    st = D.StagedDecode(w, t, host, n_slots=2, compute_stream=compute)
+    store = None
+    convert_s = 0.0
+    if compact:
+        store = D.CompactStore(w, host, n_threads=max(1, min(16, cpu_cores())))
+        c0 = time.perf_counter()
+        store.mark_written(w.lengths)
+        store.compactor.wait_idle()
+        convert_s = time.perf_counter() - c0
+    st = D.StagedDecode(w, t, host, n_slots=2, compute_stream=compute, compact=store)
     q_host = t["q"].cpu().pin_memory()
     rows_host = t["new_rows"].cpu().pin_memory()
     out_host = torch.empty(st.o.out.shape, dtype=torch.float32).pin_memory()
@@ -512,13 +536,38 @@ def run_e2e(args, w, t, dev, D, B):
     kv = w.kv_bytes_per_step()
     res = {"value": round(kv * steps / secs / 1e9, 2), "unit": UNIT,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-           "route": "host-staged, 2 arena slots, tail write-back",
+           "route": "host-staged, 2 arena slots, tail write-back"
+                    + (", published pages staged compact" if compact else ""),
            "ms_per_step": round(1e3 * secs / steps, 3),
            "h2d_GBps": round(staged_per_step * steps / secs / 1e9, 2),
            "link_probe_h2d_GBps": [round(probe_before, 2), round(probe_after, 2)],
            "link_probe": "one stream, before and after the timed steps",
            "steps": steps, "_secs": secs}
+    if compact:
+        exact_bytes = sum(run.get("n_rows", 0) * geo.row_bytes
+                          for reqs in st.exact_plan for _, _, runs in reqs for run in runs
+                          if "host_rows" in run)
+        compact_tokens = sum(run["n_pages"] * geo.page_tokens
+                             for reqs in st.plan for _, _, runs in reqs for run in runs
+                             if "host_compact" in run)
+        cnt = store.compactor.counters()
+        res["compact"] = {
+            "format": "int8 codes, one fp32 scale per (token, K|V, kv head), CRC-32 per page",
+            "pages_published": int(cnt["published_pages"]),
+            "convert_s": round(convert_s, 3),
+            "staged_bytes_exact_plan": int(exact_bytes),
+            "staged_bytes_per_step": int(st.staged_bytes_per_step()),
+            "bytes_per_token_not_moved": round((exact_bytes - st.staged_bytes_per_step())
+                                               / max(1, compact_tokens), 1),
+        }
+        if exact is not None:
+            res["compact"]["out_max_abs_vs_exact"] = float(
+                (out_host - exact[0].cpu()).abs().max())
+            res["compact"]["lse_max_abs_vs_exact"] = float(
+                (lse_host - exact[1].cpu()).abs().max())
     st.close()
+    if store is not None:
+        store.close()
     host.close()
     return res
 
