@@ -82,6 +82,14 @@ extern "C" {
 /* Thread-local message for the last failing call on this thread ("" if none). */
 const char* kv_last_error(void);
 
+/* Pinned host memory for histories and compact stores ([GMM-host]): an
+ * explicit-size cudaHostAlloc (page-locked, mapped into the device's address
+ * space), owned by the caller until kv_host_free.  Copies from it ran at a
+ * steady ~211 GB/s on GB300, against 150-200 GB/s from malloc'd memory pinned
+ * afterwards with cudaHostRegister. */
+int kv_host_alloc(size_t bytes, void** out);
+int kv_host_free(void* p);
+
 /* Library build string (compiler, target architecture). */
 const char* pa_version(void);
 

@@ -36,7 +36,7 @@ PAGE_TOKENS = 64
 
 # Every symbol pagedattn.h declares.
 EXPORTED = [
-    "kv_last_error", "pa_version",
+    "kv_last_error", "pa_version", "kv_host_alloc", "kv_host_free",
     "paged_decode_attn_lse_workspace_bytes", "paged_decode_attn_lse",
     "paged_decode_attn_lse_cuda_core", "paged_decode_attn_lse_noalloc",
     "paged_decode_attn_lse_append", "lse_merge",
@@ -204,6 +204,10 @@ def _load():
     lib.kv_last_error.argtypes = []
     lib.pa_version.restype = ctypes.c_char_p
     lib.pa_version.argtypes = []
+    lib.kv_host_alloc.restype = ctypes.c_int
+    lib.kv_host_alloc.argtypes = [ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)]
+    lib.kv_host_free.restype = ctypes.c_int
+    lib.kv_host_free.argtypes = [ctypes.c_void_p]
     lib.paged_decode_attn_lse_workspace_bytes.restype = sz
     lib.paged_decode_attn_lse_workspace_bytes.argtypes = [i32] * 5
     dec = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, sz, vp]
@@ -794,6 +798,32 @@ class Compactor:
         if getattr(self, "handle", None):
             lib.kv_compactor_destroy(self.handle)
             self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class PinnedBuffer:
+    """Pinned host memory from kv_host_alloc, viewed as a uint8 CPU tensor
+    (``.tensor``); freed by close()."""
+
+    def __init__(self, nbytes: int):
+        import numpy as np
+        ptr = ctypes.c_void_p()
+        _check(lib.kv_host_alloc(int(nbytes), ctypes.byref(ptr)))
+        self.ptr = ptr.value
+        self.nbytes = int(nbytes)
+        arr = np.ctypeslib.as_array((ctypes.c_uint8 * self.nbytes).from_address(self.ptr))
+        self.tensor = torch.from_numpy(arr)
+
+    def close(self):
+        if getattr(self, "ptr", None):
+            self.tensor = None
+            lib.kv_host_free(self.ptr)
+            self.ptr = None
 
     def __del__(self):
         try:

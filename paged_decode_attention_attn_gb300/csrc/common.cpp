@@ -45,3 +45,27 @@ extern "C" const char* kv_last_error(void) { return pa::g_message; }
 extern "C" const char* pa_version(void) {
   return "libpagedattn 0.1 (sm_103a, CUDA runtime " PA_STR(CUDART_VERSION) ")";
 }
+
+// Pinned host memory for the caller's history and compact store ("GPU memory
+// management", section "A host pool that explains its own size": the host
+// pool that owns every history is pinned and sized explicitly).
+extern "C" int kv_host_alloc(size_t bytes, void** out) {
+  pa::clear_error();
+  if (!out || bytes == 0) return pa::fail(PA_ERR_INVALID, "bytes must be > 0 and out non-null");
+  *out = nullptr;
+  const cudaError_t e = cudaHostAlloc(out, bytes, cudaHostAllocDefault);
+  if (e != cudaSuccess) {
+    *out = nullptr;
+    return pa::fail(PA_ERR_CUDA, "cudaHostAlloc of %zu bytes failed: %s", bytes,
+                    cudaGetErrorString(e));
+  }
+  return PA_OK;
+}
+
+extern "C" int kv_host_free(void* p) {
+  pa::clear_error();
+  if (!p) return PA_OK;
+  const cudaError_t e = cudaFreeHost(p);
+  return e == cudaSuccess ? PA_OK
+                          : pa::fail(PA_ERR_CUDA, "cudaFreeHost failed: %s", cudaGetErrorString(e));
+}

@@ -1049,8 +1049,12 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
 
   std::vector<Unit> units;
   units.reserve((size_t)B * T * n_kv_heads);
-  for (int bt = 0; bt < B * T; ++bt) {
-    for (int g = 0; g < n_kv_heads; ++g) {
+  // Kv-head-major order: the units of one kv head form a block of the page
+  // sequence, and every block has the same unit sizes, so the CTAs at the
+  // same offset of the n_kv_heads blocks stream the same physical pages (each
+  // its head's slice of every row) at about the same time.
+  for (int g = 0; g < n_kv_heads; ++g) {
+    for (int bt = 0; bt < B * T; ++bt) {
       Unit u{};
       u.bt_g = bt * n_kv_heads + g;
       u.tok_start = tiles[2 * bt];

@@ -135,13 +135,8 @@ class HostHistory:
             for r, L in enumerate(lengths):
                 self.offsets[(i, r)] = total
                 total += L
-        self.rows = torch.empty((total, geo.row_elems), dtype=torch.bfloat16)
-        nbytes = self.rows.numel() * 2
-        rc = torch.cuda.cudart().cudaHostRegister(self.rows.data_ptr(), nbytes, 0)
-        code = rc.value if hasattr(rc, "value") else int(rc)
-        if code != 0:
-            raise RuntimeError(f"cudaHostRegister of {nbytes} bytes failed ({rc})")
-        self._registered = True
+        self._mem = B.PinnedBuffer(total * geo.row_bytes)
+        self.rows = self._mem.tensor.view(torch.bfloat16).view(total, geo.row_elems)
         for i in range(len(self.layers)):
             for r, L in enumerate(lengths):
                 off = self.offsets[(i, r)]
@@ -158,9 +153,10 @@ class HostHistory:
         return self.rows[self.offsets[(i, r)] + row]
 
     def close(self):
-        if getattr(self, "_registered", False):
-            torch.cuda.cudart().cudaHostUnregister(self.rows.data_ptr())
-            self._registered = False
+        if getattr(self, "_mem", None) is not None:
+            self.rows = None
+            self._mem.close()
+            self._mem = None
 
     def __del__(self):
         try:
@@ -189,12 +185,8 @@ class CompactStore:
             for r in range(w.batch):
                 self.offsets[(i, r)] = total
                 total += w.max_pages * self.page_bytes
-        self.buf = torch.empty(total, dtype=torch.uint8)
-        rc = torch.cuda.cudart().cudaHostRegister(self.buf.data_ptr(), total, 0)
-        code = rc.value if hasattr(rc, "value") else int(rc)
-        if code != 0:
-            raise RuntimeError(f"cudaHostRegister of {total} bytes failed ({rc})")
-        self._registered = True
+        self._mem = B.PinnedBuffer(total)
+        self.buf = self._mem.tensor
         exact = [host.row_address(i, r, 0) for i in range(self.n_layers) for r in range(w.batch)]
         comp = [self.buf.data_ptr() + self.offsets[(i, r)]
                 for i in range(self.n_layers) for r in range(w.batch)]
@@ -218,9 +210,10 @@ class CompactStore:
         if getattr(self, "compactor", None) is not None:
             self.compactor.close()
             self.compactor = None
-        if getattr(self, "_registered", False):
-            torch.cuda.cudart().cudaHostUnregister(self.buf.data_ptr())
-            self._registered = False
+        if getattr(self, "_mem", None) is not None:
+            self.buf = None
+            self._mem.close()
+            self._mem = None
 
     def __del__(self):
         try:
