@@ -580,42 +580,68 @@ def run_bus_model(args):
     from paged_decode_attention_attn_gb300 import decode as D
     from paged_decode_attention_attn_gb300 import workloads as wl
     dev = torch.device("cuda", 0)
-    points, rows = [], []
-    for L in (32768, 65536, 131072, 262144):
+    def measure(L, compact):
         w = wl.custom([L], [[(0, L)]], seed=31, n_layers=args.layers, n_spare=2)
         t = wl.materialize(w, dev)
         host = D.HostHistory(w, t)
-        st = D.StagedDecode(w, t, host, n_slots=2)
+        store = None
+        if compact:
+            store = D.CompactStore(w, host, n_threads=max(1, min(16, cpu_cores())))
+            store.mark_written(w.lengths)
+            store.compactor.wait_idle()
+        st = D.StagedDecode(w, t, host, n_slots=2, compact=store)
         for _ in range(2):
             st.step()
         st.drain()
         torch.cuda.synchronize(dev)
-        n = 5
-        t0 = time.perf_counter()
-        for _ in range(n):
+        # median of single-step times: the host side is shared, and a
+        # neighbour's burst on the link must not bend the fit
+        times = []
+        for _ in range(7):
+            t0 = time.perf_counter()
             st.step()
-        st.drain()
-        torch.cuda.synchronize(dev)
-        secs = (time.perf_counter() - t0) / n
+            st.drain()
+            torch.cuda.synchronize(dev)
+            times.append(time.perf_counter() - t0)
+        secs = statistics.median(times)
         stats = st.handle.stats()
         staged = stats.staged_bytes // stats.stage_generation * w.n_layers
-        points.append((staged, secs))
-        rows.append({"ctx": L, "staged_bytes": int(staged), "step_ms": round(1e3 * secs, 3)})
         st.close()
+        if store is not None:
+            store.close()
         host.close()
         del st, host, t
         torch.cuda.empty_cache()
+        return staged, secs
+
+    points, rows = [], []
+    contexts = (32768, 65536, 131072, 262144)
+    for L in contexts:
+        staged, secs = measure(L, False)
+        points.append((staged, secs))
+        rows.append({"ctx": L, "staged_bytes": int(staged), "step_ms": round(1e3 * secs, 3)})
     model = bm.fit(points)
     ends = bm.fit([points[0], points[-1]])
     for r, e in zip(rows, bm.relative_errors(model, points)):
         r["fit_error_pct"] = round(100 * e, 3)
+    # the compact route predicted from its bytes alone by the model fitted above
+    compact_rows = []
+    if not args.no_compact:
+        for L in contexts:
+            staged, secs = measure(L, True)
+            pred = model.predict(staged)
+            compact_rows.append({"ctx": L, "staged_bytes": int(staged),
+                                 "step_ms": round(1e3 * secs, 3),
+                                 "predicted_ms": round(1e3 * pred, 3),
+                                 "error_pct": round(100 * (pred - secs) / secs, 3)})
     print(json.dumps({
         "bus_model": {k: round(v, 4) for k, v in model.as_dict().items()},
         "worst_error_pct": round(100 * bm.worst_relative_error(model, points), 3),
         "endpoint_model": {k: round(v, 4) for k, v in ends.as_dict().items()},
         "endpoint_model_worst_error_pct":
             round(100 * bm.worst_relative_error(ends, points), 3),
-        "points": rows, "layers": args.layers, "route": "host-staged, 2 arena slots"}),
+        "points": rows, "layers": args.layers, "route": "host-staged, 2 arena slots",
+        "compact_points": compact_rows}),
         flush=True)
 
 

@@ -277,7 +277,7 @@ typedef struct {
     uint32_t     flags;           /* PA_ARENA_* */
     /* Compact runs ([KVE-exact] "runs of two representations"; optional): a
      * staged compact page lands in the slot's landing area and is expanded on
-     * the H2D stream into a full bf16 page of the slot.  0 / 0 / 0: refused. */
+     * the compute stream into a full bf16 page of the slot.  0 / 0 / 0: refused. */
     int32_t      compact_head_dim;  /* head_dim of the compact format            */
     uint64_t     landing_offset;    /* bytes from device_base to slot 0's landing
                                        area (256-B aligned, after every page)    */
@@ -346,9 +346,10 @@ int kv_arena_drain(kv_arena* arena);
  * (staged runs, exact or compact, get consecutive slot pages in request/run
  * order), records the slot's copy event and makes the compute stream wait on
  * it.  A compact run is copied into the slot's landing area and expanded, on
- * the H2D stream before the copy event, into bf16 pages holding
- * bf16_rne(c * s) (the values the compact page stands for); the attention then
- * reads it like any page.  PA_ERR_ORDER if the slot's previous stage was never
+ * the compute stream after that wait (so the H2D stream moves on to the next
+ * layer), into bf16 pages holding bf16_rne(c * s) (the values the compact
+ * page stands for); an attention enqueued next on the compute stream reads it
+ * like any page.  PA_ERR_ORDER if the slot's previous stage was never
  * marked attention-done.
  *   *slot_out        the slot used; *page_table_out its device page table
  *                    ([max_requests][max_pages]) to pass to the attention. */

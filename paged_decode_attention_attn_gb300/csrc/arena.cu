@@ -458,6 +458,21 @@ int submit_stage(kv_arena* a, int slot, bool wait_prior_readers, const kv_stage_
     }
     records->push_back(std::move(rec));
   }
+  int32_t* table = d.page_tables + (size_t)slot * d.max_requests * d.max_pages;
+  for (size_t r0 = 0; r0 < table_runs.size(); r0 += kMaxRunsPerLaunch) {
+    TableParams tp{};
+    tp.table = table;
+    tp.max_pages = d.max_pages;
+    tp.n_runs = static_cast<int>(std::min<size_t>(kMaxRunsPerLaunch, table_runs.size() - r0));
+    std::memcpy(tp.runs, table_runs.data() + r0, tp.n_runs * sizeof(TableRun));
+    if ((rc = op_table(a, h2d, slot, tp)) != PA_OK) return rc;
+  }
+  if ((rc = op_record(a, h2d, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
+  if ((rc = op_wait(a, d.compute_stream, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
+  // Compact runs are expanded on the compute stream, after the copy event and
+  // before the attention: the H2D stream is free to copy the next layer
+  // meanwhile, and the slot's landing area is rewritten only after this
+  // layer's attention (the slot-reuse wait), hence after its expansion.
   for (size_t r0 = 0; r0 < expand_runs.size(); r0 += kMaxRunsPerLaunch) {
     ExpandParams ep{};
     ep.landing = landing;
@@ -474,19 +489,8 @@ int submit_stage(kv_arena* a, int slot, bool wait_prior_readers, const kv_stage_
       rows += (long long)ep.runs[k].n_pages * d.page_tokens;
     }
     ep.total_rows = rows;
-    if ((rc = op_expand(a, h2d, slot, ep)) != PA_OK) return rc;
+    if ((rc = op_expand(a, d.compute_stream, slot, ep)) != PA_OK) return rc;
   }
-  int32_t* table = d.page_tables + (size_t)slot * d.max_requests * d.max_pages;
-  for (size_t r0 = 0; r0 < table_runs.size(); r0 += kMaxRunsPerLaunch) {
-    TableParams tp{};
-    tp.table = table;
-    tp.max_pages = d.max_pages;
-    tp.n_runs = static_cast<int>(std::min<size_t>(kMaxRunsPerLaunch, table_runs.size() - r0));
-    std::memcpy(tp.runs, table_runs.data() + r0, tp.n_runs * sizeof(TableRun));
-    if ((rc = op_table(a, h2d, slot, tp)) != PA_OK) return rc;
-  }
-  if ((rc = op_record(a, h2d, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
-  if ((rc = op_wait(a, d.compute_stream, "copy", slot, a->ev_copy[slot])) != PA_OK) return rc;
   return PA_OK;
 }
 

@@ -226,7 +226,7 @@ def make_compact_arena(B, n_slots=2, slot_pages=8, window_pages=4, landing_pages
                    landing_bytes=landing)
 
 
-def test_compact_runs_land_then_expand_before_the_copy_event(B):
+def test_compact_runs_land_then_expand_on_the_compute_stream(B):
     a = make_compact_arena(B)
     a.stage_layer(0, [(0, 7, [compact(0, 3, 0x1000), staged(3, 2, 0x9000, rows=100)]),
                       (1, 9, [compact(0, 1, 0x5000), resident(1, 1, 2)])])
@@ -234,16 +234,16 @@ def test_compact_runs_land_then_expand_before_the_copy_event(B):
         "h2d copy h2d bytes=399360 page=4 row=-1",
         "h2d copy h2d bytes=409600 page=7 row=0",
         "h2d copy h2d bytes=133120 page=9 row=-1",
-        "h2d expand slot=0 runs=2 +0:3->4 +399360:1->9",
         "h2d table slot=0 runs=4 0:0+3->4 0:3+2->7 1:0+1->9 1:1+1->2",
         "h2d record copy[0]",
         "compute wait copy[0]",
+        "compute expand slot=0 runs=2 +0:3->4 +399360:1->9",
     ]
     assert a.stats().staged_bytes == 399360 + 409600 + 133120
     # slot 1's landing area follows slot 0's
     a.mark_attention_done(0)
     a.stage_layer(1, [(0, 7, [compact(0, 2, 0x1000)])])
-    assert a.call_log()[-4] == "h2d expand slot=1 runs=1 +0:2->12"
+    assert a.call_log()[-1] == "compute expand slot=1 runs=1 +0:2->12"
 
 
 def test_compact_runs_are_checked(B):
