@@ -594,8 +594,9 @@ def run_bus_model(args):
             st.step()
         st.drain()
         torch.cuda.synchronize(dev)
-        # median of single-step times: the host side is shared, and a
-        # neighbour's burst on the link must not bend the fit
+        # fastest of single-step times: the host side is shared, and a
+        # neighbour's burst on the link (seen to stretch single steps by
+        # 40-90%) must not bend the fit; the median is reported beside it
         times = []
         for _ in range(7):
             t0 = time.perf_counter()
@@ -603,7 +604,8 @@ def run_bus_model(args):
             st.drain()
             torch.cuda.synchronize(dev)
             times.append(time.perf_counter() - t0)
-        secs = statistics.median(times)
+        secs = min(times)
+        med_secs[(L, compact)] = statistics.median(times)
         stats = st.handle.stats()
         staged = stats.staged_bytes // stats.stage_generation * w.n_layers
         st.close()
@@ -615,11 +617,13 @@ def run_bus_model(args):
         return staged, secs
 
     points, rows = [], []
+    med_secs = {}
     contexts = (32768, 65536, 131072, 262144)
     for L in contexts:
         staged, secs = measure(L, False)
         points.append((staged, secs))
-        rows.append({"ctx": L, "staged_bytes": int(staged), "step_ms": round(1e3 * secs, 3)})
+        rows.append({"ctx": L, "staged_bytes": int(staged), "step_ms": round(1e3 * secs, 3),
+                     "median_step_ms": round(1e3 * med_secs[(L, False)], 3)})
     model = bm.fit(points)
     ends = bm.fit([points[0], points[-1]])
     for r, e in zip(rows, bm.relative_errors(model, points)):
@@ -632,6 +636,7 @@ def run_bus_model(args):
             pred = model.predict(staged)
             compact_rows.append({"ctx": L, "staged_bytes": int(staged),
                                  "step_ms": round(1e3 * secs, 3),
+                                 "median_step_ms": round(1e3 * med_secs[(L, True)], 3),
                                  "predicted_ms": round(1e3 * pred, 3),
                                  "error_pct": round(100 * (pred - secs) / secs, 3)})
     print(json.dumps({
@@ -641,6 +646,7 @@ def run_bus_model(args):
         "endpoint_model_worst_error_pct":
             round(100 * bm.worst_relative_error(ends, points), 3),
         "points": rows, "layers": args.layers, "route": "host-staged, 2 arena slots",
+        "timing": "fastest of 7 single steps per point (median beside it)",
         "compact_points": compact_rows}),
         flush=True)
 
