@@ -425,13 +425,24 @@ class PlannedDecode:
     memory (after the previous step's attention and write-back are done with
     the pool pages they reuse), and each layer stages every page that is not
     hot.  Contexts are the workload's requests; all run every step.
+
+    With a CompactStore, the hot window stays exact and every cold page that
+    the background converter has published is staged compact ("KV-cache
+    engineering", section "Exact recent pages, compact older pages").  A page
+    is handed to the converter only once the device event recorded after the
+    write-backs that completed it has fired (checked without blocking at the
+    next step), so it is fully written in every layer, in host memory.
     """
 
     def __init__(self, w: DecodeWorkload, t: dict, host: HostHistory, planner,
-                 targets, bursts, n_slots: int = 2, compute_stream=None, fused: bool = True):
+                 targets, bursts, n_slots: int = 2, compute_stream=None, fused: bool = True,
+                 compact: CompactStore | None = None):
         geo = w.geometry
         self.w, self.t, self.host, self.planner = w, t, host, planner
         self.fused = fused
+        self.compact = compact
+        self.pending = []          # (event after a step's write-backs, full pages per request)
+        self.compact_used = {}     # this step's compact-staged pages per (layer, request)
         self.n_layers = t["pool"].shape[0]
         dev = t["pool"].device
         self.dev = dev
@@ -442,16 +453,26 @@ class PlannedDecode:
         self.win_pages = self.n_layers * self.pool_pages
         self.slot_pages = max(1, sum(w.pages_of(r) for r in range(w.batch)))
         arena_pages = self.win_pages + n_slots * self.slot_pages
-        self.arena = torch.full((arena_pages, geo.page_tokens, geo.row_elems), float("nan"),
-                                dtype=torch.bfloat16, device=dev)
+        page_bytes = geo.page_tokens * geo.row_bytes
+        landing = 0
+        if compact is not None:
+            landing = -(-self.slot_pages * compact.page_bytes // 256) * 256
+        self.arena_buf = torch.empty(arena_pages * page_bytes + n_slots * landing,
+                                     dtype=torch.uint8, device=dev)
+        self.arena = self.arena_buf[: arena_pages * page_bytes].view(torch.bfloat16).view(
+            arena_pages, geo.page_tokens, geo.row_elems)
+        self.arena.fill_(float("nan"))
         self.page_tables = torch.zeros((n_slots, w.batch, w.max_pages), dtype=torch.int32,
                                        device=dev)
         torch.cuda.synchronize(dev)
-        self.handle = B.Arena(self.arena.data_ptr(), self.arena.numel() * 2, geo.row_bytes,
+        self.handle = B.Arena(self.arena_buf.data_ptr(), self.arena_buf.numel(), geo.row_bytes,
                               n_slots, self.win_pages, self.slot_pages,
                               self.page_tables.data_ptr(), w.batch, w.max_pages,
                               compute_stream=self.compute, h2d_stream=self.h2d,
-                              d2h_stream=self.d2h)
+                              d2h_stream=self.d2h,
+                              compact_head_dim=geo.head_dim if compact is not None else 0,
+                              landing_offset=arena_pages * page_bytes if landing else 0,
+                              landing_bytes=landing)
         for r in range(w.batch):
             planner.admit(r, int(targets[r]), int(bursts[r]))
         self.step_done = torch.cuda.Event()
@@ -490,13 +511,15 @@ class PlannedDecode:
                                              self.host.offsets[(i, r)] + hi]
                         self.arena[page, : hi - lo].copy_(src, non_blocking=True)
 
-    def _runs(self, i, r, L):
+    def _runs(self, i, r, L, published=None):
         """Page runs of request r for layer i: hot pages from the pool,
-        maximal runs of cold pages staged from the host."""
+        maximal runs of cold pages staged from the host (compact where
+        ``published`` says the converter has published the page)."""
         pt = self.w.geometry.page_tokens
         n = -(-L // pt)
         res = self.resident[r]
         runs, lp = [], 0
+        used = self.compact_used.setdefault((i, r), [])
         while lp < n:
             if lp in res:
                 runs.append(dict(logical_page=lp, n_pages=1,
@@ -504,12 +527,27 @@ class PlannedDecode:
                 lp += 1
                 continue
             start = lp
-            while lp < n and lp not in res:
+            kind = bool(published and published[lp])
+            while lp < n and lp not in res and bool(published and published[lp]) == kind:
                 lp += 1
+            if kind:
+                runs.append(dict(logical_page=start, n_pages=lp - start,
+                                 n_rows=(lp - start) * pt,
+                                 host_compact=self.compact.address(i, r, start)))
+                used.extend(range(start, lp))
+                continue
             rows = min(lp * pt, L - 1) - start * pt
             runs.append(dict(logical_page=start, n_pages=lp - start, n_rows=max(0, rows),
                              host_rows=self.host.row_address(i, r, start * pt)))
         return runs
+
+    def _publish_written(self):
+        """Hand the converter every page completed by steps whose write-backs
+        have finished (a non-blocking event query per pending step)."""
+        while self.pending and self.pending[0][0].query():
+            _, full = self.pending.pop(0)
+            for r, f in enumerate(full):
+                self.compact.compactor.mark_written(r, f)
 
     def step(self, lengths):
         """One decode step at the given lengths (tokens, including the new one)."""
@@ -518,11 +556,17 @@ class PlannedDecode:
         if not all(admitted):
             raise RuntimeError(f"planner refused contexts {admitted}")
         self.resident = [self.planner.resident(r) for r in range(w.batch)]
+        published = None
+        self.compact_used = {}
+        if self.compact is not None:
+            self._publish_written()
+            published = [self.compact.published(r) for r in range(w.batch)]
         self._copy_in(lengths)
         tiles = np.zeros((w.batch, 1, 2), dtype=np.int32)
         tiles[:, 0, 1] = lengths
         for i in range(self.n_layers):
-            reqs = [(r, (i << 32) | r, self._runs(i, r, int(lengths[r])))
+            reqs = [(r, (i << 32) | r,
+                     self._runs(i, r, int(lengths[r]), published[r] if published else None))
                     for r in range(w.batch)]
             slot, _ = self.handle.stage_layer(i, reqs)
             _layer_kernels(self.fused, False, t["q"][i], self.arena, self.page_tables[slot],
@@ -536,6 +580,11 @@ class PlannedDecode:
         self.step_done.record(self.compute)
         self.wb_done.record(self.d2h)
         self.have_prev = True
+        if self.compact is not None:
+            ev = torch.cuda.Event()
+            ev.record(self.d2h)
+            pt = geo.page_tokens
+            self.pending.append((ev, [int(L) // pt for L in lengths]))
 
     def kernel_status(self) -> int:
         return int(self.workspace[:4].view(torch.int32).item()) | int(self.status.item())

@@ -41,11 +41,12 @@ def clone(t):
     return {k: v.clone() for k, v in t.items()}
 
 
-def run_both(D, w, t):
+def run_both(D, w, t, kv_ready=False):
     poison_new_rows(w, t)
     tf, tu = clone(t), clone(t)
-    fused = D.ResidentDecode(w, tf, fused=True)
+    fused = D.ResidentDecode(w, tf, fused=True, kv_ready=kv_ready)
     unfused = D.ResidentDecode(w, tu, fused=False)
+    torch.cuda.synchronize()     # the clones' kernels are complete
     fused.step()
     unfused.step()
     torch.cuda.synchronize()
@@ -100,16 +101,18 @@ def test_fused_equals_two_launches_at_full_size(D, make):
     torch.cuda.empty_cache()
 
 
-def test_fused_over_several_launches(D):
+@pytest.mark.parametrize("kv_ready", [False, True], ids=["wait", "early-loads"])
+def test_fused_over_several_launches(D, kv_ready):
     # 80 requests x 4 tiles x 4 kv heads = 1,280 units: the library issues two
-    # launches, and only the first stores the new rows.
+    # launches, and only the first stores the new rows (the second may load
+    # the pages the first writes early: it substitutes the rows anyway).
     rng = np.random.default_rng(4)
     lengths = rng.integers(1, 400, size=80)
     tiles = [[(0, int(L)), (0, int(L) // 2), (int(L) // 2, int(L)), (max(0, int(L) - 7), int(L))]
              for L in lengths]
     w = wl.custom(lengths, tiles, seed=8, n_spare=3)
     t = wl.materialize(w, "cuda")
-    fused, unfused, tf, tu = run_both(D, w, t)
+    fused, unfused, tf, tu = run_both(D, w, t, kv_ready=kv_ready)
     assert fused.kernel_status() == 0 and unfused.kernel_status() == 0
     assert_same(fused, unfused, tf, tu)
 
