@@ -245,7 +245,7 @@ def oracle_sample(n_tasks, workers, length=31744):
 
 
 def cpu_baseline_dict(workers_arg):
-    workers = workers_arg or min(8, cpu_cores())
+    workers = workers_arg or cpu_cores()
     s = oracle_sample(n_tasks=2 * workers, workers=workers)
     gbs = s["kv_bytes"] / s["busy_s"] * workers / 1e9
     return {"value": round(gbs, 4), "unit": UNIT, "cores": workers, "kind": "oracle",
@@ -261,7 +261,7 @@ def run_reference(args, budget_s=150.0):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    workers = args.cpu_workers or min(8, cpu_cores())
+    workers = args.cpu_workers or cpu_cores()
     probe = oracle_sample(n_tasks=workers, workers=workers, length=4096)
     per_token_wall = probe["wall_s"] / 4096
     steps_total = args.steps + args.warmup
