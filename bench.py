@@ -398,6 +398,7 @@ def run_ours(args):
     peak, peak_kind = hbm_peak()
     kern_ms = statistics.mean(kernel_ms)
     achieved = kv_bytes_layer / (kern_ms / 1e3) / 1e9
+    null_ms = null_arm(args, w, t, D, B, dev, fused, kv_ready)
 
     # ---- staged route, end to end through host buffers ----
     e2e = e2e_compact = None
@@ -443,12 +444,16 @@ def run_ours(args):
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": round(achieved / peak, 4),
+                         "frac_of_nominal_8000": round(achieved / 8000.0, 4),
                          "traffic": recorded_traffic() if args.workload == "4x31744" else None,
                          "kernel": "paged_decode_kernel",
                          "bytes_per_launch": kv_bytes_layer,
                          "mean_launch_ms": round(kern_ms, 5)},
             "clocks": clk,
             "host_issue_ms_per_step": round(1e3 * host_issue_s / args.steps, 4),
+            "null_arm": {"ms_per_step": round(null_ms, 4),
+                         "what": "the same launches with one-token tiles (the new token "
+                                 "only): the step's fixed cost, outside the timed region"},
             "step_launch": f"CUDA graph of the {launches_per_step} launches of one step, "
                            "replayed per step",
         }
@@ -462,6 +467,58 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def null_arm(args, w, t, D, B, dev, fused, kv_ready):
+    """Per-step time of the same launches over one-token tiles (the new token
+    of every request only), replayed as a CUDA graph: the fixed cost of a
+    step, for comparison with the timed one."""
+    import numpy as np
+    import torch
+    geo = w.geometry
+    tiles = np.zeros((w.batch, 1, 2), dtype=np.int32)
+    tiles[:, 0, 0] = w.lengths - 1
+    tiles[:, 0, 1] = w.lengths
+    nd = D.ResidentDecode(w, t, cuda_core=args.cuda_core, tiles=tiles)
+    o = nd.o
+
+    def step(s):
+        for i in range(w.n_layers):
+            if fused:
+                B.paged_decode_attn_lse_append(t["q"][i], t["pool"][i], t["page_table"],
+                                               nd.tiles, geo.scale, t["positions"],
+                                               t["new_rows"][i], o.tile_out[i], o.tile_lse[i],
+                                               nd.workspace, stream=s, kv_ready=kv_ready)
+            else:
+                B.kv_append_rows(t["pool"][i], t["page_table"], t["positions"],
+                                 t["new_rows"][i], status=nd.status, stream=s)
+                B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], nd.tiles,
+                                        geo.scale, o.tile_out[i], o.tile_lse[i], nd.workspace,
+                                        stream=s, cuda_core=args.cuda_core)
+
+    stream = torch.cuda.current_stream(dev)
+    torch.cuda.synchronize(dev)
+    for _ in range(3):
+        step(stream)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream(dev)
+    cap.wait_stream(stream)
+    with torch.cuda.graph(graph, stream=cap):
+        step(cap)
+    torch.cuda.synchronize(dev)
+    for _ in range(3):
+        graph.replay()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    n = 200
+    e0.record(stream)
+    for _ in range(n):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if nd.kernel_status() != 0:
+        raise RuntimeError("null arm kernel status non-zero")
+    return e0.elapsed_time(e1) / n
 
 
 def run_e2e(args, w, t, dev, D, B, compact=False, exact=None):
