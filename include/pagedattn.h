@@ -217,6 +217,18 @@ int paged_decode_attn_lse_append(const void* q, void* pool, int64_t pool_pages,
                                  void* workspace, size_t workspace_bytes,
                                  unsigned flags, cudaStream_t stream);
 
+/* Test hook for failure detection (no counterpart in the source pages): the
+ * next decode call made on this thread (any paged_decode_attn_lse* entry
+ * point) gives every bounded device wait up after wait_limit_ns (instead of
+ * 2 s), and CTA 0 leaves its page load number `iteration` unarmed, so the
+ * wait for that page runs out: the kernel sets PA_STATUS_TIMEOUT, lets the
+ * loads it issued land and returns; the context stays usable.  Outputs of
+ * that call are invalid and its workspace must be zero-filled again before
+ * reuse.  (-1, 0) clears a pending setting.  PA_ERR_INVALID otherwise unless
+ * iteration >= 0 and 0 < wait_limit_ns <= 2 s.  Nothing else calls it;
+ * production calls never stall. */
+int paged_decode_attn_test_stall(int iteration, uint64_t wait_limit_ns);
+
 /* ------------------------------------------------------------------------ */
 /* FP32 LSE merge  ([KVE-exact])                                            */
 /* ------------------------------------------------------------------------ */

@@ -39,7 +39,7 @@ EXPORTED = [
     "kv_last_error", "pa_version", "kv_host_alloc", "kv_host_free",
     "paged_decode_attn_lse_workspace_bytes", "paged_decode_attn_lse",
     "paged_decode_attn_lse_cuda_core", "paged_decode_attn_lse_noalloc",
-    "paged_decode_attn_lse_append", "lse_merge",
+    "paged_decode_attn_lse_append", "paged_decode_attn_test_stall", "lse_merge",
     "kv_append_rows",
     "kv_arena_create", "kv_arena_destroy", "kv_arena_drain", "kv_stage_layer",
     "kv_mark_attention_done", "kv_writeback_tail", "kv_arena_get_stats",
@@ -221,6 +221,8 @@ def _load():
     lib.paged_decode_attn_lse_append.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32,
                                                  i32, ctypes.c_float, vp, vp, vp, vp, vp, sz,
                                                  ctypes.c_uint, vp]
+    lib.paged_decode_attn_test_stall.restype = i32
+    lib.paged_decode_attn_test_stall.argtypes = [i32, ctypes.c_uint64]
     lib.lse_merge.restype = i32
     lib.lse_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
     lib.kv_append_rows.restype = i32
@@ -429,6 +431,12 @@ def paged_decode_attn_lse_append(q, pool, page_table, tiles, scale, positions, n
         _dev(new_rows, torch.bfloat16, "new_rows"), _dev(out, torch.float32, "out"),
         _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"),
         workspace.numel(), PA_DECODE_KV_READY if kv_ready else 0, _stream_handle(stream)))
+
+
+def test_stall(iteration: int, wait_limit_ns: int):
+    """Failure-detection test hook: the next decode call on this thread stalls
+    CTA 0 at page load ``iteration`` and gives waits up after wait_limit_ns."""
+    _check(lib.paged_decode_attn_test_stall(int(iteration), int(wait_limit_ns)))
 
 
 def lse_merge(out_parts, lse_parts, part_offsets, out, lse, stream=None):

@@ -127,6 +127,11 @@ struct Params {
   // precedes this one in the stream runs: the producer may issue its first
   // kStages page loads before the grid dependency wait.
   int kv_ready;
+  // Bounded device waits give up after wait_limit_ns (PA_STATUS_TIMEOUT).
+  // stall_iteration >= 0 (test hook only): CTA 0's producer leaves that
+  // stage unarmed, so its consumers' wait runs out.
+  unsigned long long wait_limit_ns;
+  int stall_iteration;
   Unit units[kMaxUnits];
 };
 
@@ -336,7 +341,7 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
             const int s = it % kStages;
             if (it >= kStages) {
               good = ptx::mbar_wait_bounded(sh.empty_bar + 8 * s, ((it / kStages) - 1) & 1,
-                                            kWaitLimitNs) ? 1 : 0;
+                                            p.wait_limit_ns) ? 1 : 0;
             }
             if (good) {
               const bool bad = pid < 0 || (long long)pid >= p.pool_pages;
@@ -345,12 +350,15 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
               const int y = (bad ? 0 : pid) * kPage;
               const uint32_t full = sh.full_bar + 8 * s;
               const uint32_t dst = ptx::smem_addr(sh.stages + s * kStageBytes);
-              ptx::mbar_arrive_expect_tx(full, kStageBytes);
+              if (it != p.stall_iteration || blockIdx.x != 0) {
+                ptx::mbar_arrive_expect_tx(full, kStageBytes);
 #pragma unroll
-              for (int c = 0; c < kD / kBoxCols; ++c) {
-                ptx::tma_load_2d_hint(dst + c * kBoxBytes, &tmap, xk + c * kBoxCols, y, full, pol);
-                ptx::tma_load_2d_hint(dst + kHalfBytes + c * kBoxBytes, &tmap, xv + c * kBoxCols,
-                                      y, full, pol);
+                for (int c = 0; c < kD / kBoxCols; ++c) {
+                  ptx::tma_load_2d_hint(dst + c * kBoxBytes, &tmap, xk + c * kBoxCols, y, full,
+                                        pol);
+                  ptx::tma_load_2d_hint(dst + kHalfBytes + c * kBoxBytes, &tmap,
+                                        xv + c * kBoxCols, y, full, pol);
+                }
               }
             } else {
               atomicOr(p.status, PA_STATUS_TIMEOUT);
@@ -372,7 +380,8 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     if (!ok && lane == 0) {
       // Let the copies already issued land before the CTA can exit.
       for (int k = max(0, it - kStages); k < it; ++k) {
-        ptx::mbar_wait_bounded(sh.full_bar + 8 * (k % kStages), (k / kStages) & 1, kWaitLimitNs);
+        ptx::mbar_wait_bounded(sh.full_bar + 8 * (k % kStages), (k / kStages) & 1,
+                               p.wait_limit_ns);
       }
     }
     return;
@@ -470,7 +479,7 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
 
       for (int lp = lo; lp < hi; ++lp, ++it) {
         const int s = it % kStages;
-        if (!ptx::mbar_wait_bounded(sh.full_bar + 8 * s, (it / kStages) & 1, kWaitLimitNs)) {
+        if (!ptx::mbar_wait_bounded(sh.full_bar + 8 * s, (it / kStages) & 1, p.wait_limit_ns)) {
           if (lane == 0) {
             atomicOr(p.status, PA_STATUS_TIMEOUT);
             *sh.abort_flag = 1;
@@ -646,7 +655,7 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       const int lane_chunk = lane & 7;
       for (int lp = lo; lp < hi; ++lp, ++it) {
         const int s = it % kStages;
-        if (!ptx::mbar_wait_bounded(sh.full_bar + 8 * s, (it / kStages) & 1, kWaitLimitNs)) {
+        if (!ptx::mbar_wait_bounded(sh.full_bar + 8 * s, (it / kStages) & 1, p.wait_limit_ns)) {
           if (lane == 0) {
             atomicOr(p.status, PA_STATUS_TIMEOUT);
             *sh.abort_flag = 1;
@@ -985,6 +994,11 @@ int launch_units(const CUtensorMap& tmap, const std::vector<Unit>& units, size_t
   return PA_OK;
 }
 
+// Test hook state (paged_decode_attn_test_stall): consumed by the next run()
+// on the calling thread.
+thread_local int t_stall_iteration = -1;
+thread_local unsigned long long t_wait_limit_ns = 0;
+
 int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
         const int32_t* page_table, int max_pages, const int32_t* tiles, int B, int T,
         int n_q_heads, int n_kv_heads, int head_dim, float scale, float* out, float* lse,
@@ -1086,6 +1100,10 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
   common.positions = positions;
   common.row_elems = row_elems;
   common.kv_ready = (flags & PA_DECODE_KV_READY) ? 1 : 0;
+  common.wait_limit_ns = t_wait_limit_ns ? t_wait_limit_ns : kWaitLimitNs;
+  common.stall_iteration = t_stall_iteration;
+  t_stall_iteration = -1;
+  t_wait_limit_ns = 0;
 
   // Launches of at most kMaxUnitsLarge units each; every launch partitions its
   // own pages and reuses the workspace after the previous one (same stream).
@@ -1273,5 +1291,21 @@ extern "C" int paged_decode_attn_lse_noalloc(const void* q, const void* pool, in
     if (c != cudaSuccess)
       return pa::fail(PA_ERR_CUDA, "copying the status word failed: %s", cudaGetErrorString(c));
   }
+  return PA_OK;
+}
+
+extern "C" int paged_decode_attn_test_stall(int iteration, uint64_t wait_limit_ns) {
+  pa::clear_error();
+  if (iteration == -1 && wait_limit_ns == 0) {   // clear a pending setting
+    pa::decode::t_stall_iteration = -1;
+    pa::decode::t_wait_limit_ns = 0;
+    return PA_OK;
+  }
+  if (iteration < 0 || wait_limit_ns == 0 || wait_limit_ns > pa::decode::kWaitLimitNs)
+    return pa::fail(PA_ERR_INVALID,
+                    "iteration must be >= 0 and wait_limit_ns in (0, %llu]",
+                    (unsigned long long)pa::decode::kWaitLimitNs);
+  pa::decode::t_stall_iteration = iteration;
+  pa::decode::t_wait_limit_ns = wait_limit_ns;
   return PA_OK;
 }

@@ -106,3 +106,12 @@ def test_fused_append_argument_checks(B):
     assert "new_rows" in B.last_error()
     assert call(fake, fake, flags=2) == B.PA_ERR_INVALID
     assert "flags" in B.last_error()
+
+
+def test_stall_hook_argument_checks(B):
+    assert B.lib.paged_decode_attn_test_stall(-1, 1000) == B.PA_ERR_INVALID
+    assert B.lib.paged_decode_attn_test_stall(0, 0) == B.PA_ERR_INVALID
+    assert B.lib.paged_decode_attn_test_stall(0, 3_000_000_000) == B.PA_ERR_INVALID
+    # a valid setting applies to the next call on this thread only; clear it
+    assert B.lib.paged_decode_attn_test_stall(2, 50_000_000) == B.PA_OK
+    assert B.lib.paged_decode_attn_test_stall(-1, 0) == B.PA_OK
