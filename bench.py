@@ -327,7 +327,8 @@ def run_ours(args):
     # launch may load its first pages while the previous kernel finishes.
     kv_ready = fused and not args.no_early_kv
     merge = w.n_tiles > 1       # one tile per request: the merge is the identity
-    launches_per_step = (1 + int(merge) + int(not fused)) * w.n_layers
+    # the fused launch also merges the tiles; unfused: tail write, attention, merge
+    launches_per_step = (1 if fused else 2 + int(merge)) * w.n_layers
 
     def resident_step(step_idx, s):
         o = res.o
@@ -341,14 +342,16 @@ def run_ours(args):
                 B.paged_decode_attn_lse_append(t["q"][i], t["pool"][i], t["page_table"],
                                                res.tiles, geo.scale, t["positions"],
                                                t["new_rows"][i], o.tile_out[i], o.tile_lse[i],
-                                               res.workspace, stream=s, kv_ready=kv_ready)
+                                               res.workspace, stream=s, kv_ready=kv_ready,
+                                               merged_out=o.out[i] if merge else None,
+                                               merged_lse=o.lse[i] if merge else None)
             else:
                 B.paged_decode_attn_lse(t["q"][i], t["pool"][i], t["page_table"], res.tiles,
                                         geo.scale, o.tile_out[i], o.tile_lse[i], res.workspace,
                                         stream=s, cuda_core=args.cuda_core)
             if step_idx is not None:
                 ev[step_idx * w.n_layers + i][1].record(s)
-            if merge:
+            if merge and not fused:
                 B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
                             o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
                             o.lse[i], stream=s)
@@ -435,7 +438,7 @@ def run_ours(args):
                        "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step)",
                        "kernel": "cuda-core fp32" if args.cuda_core
                        else "tensor-core mma.sync bf16 + TMA pipeline"
-                       + (", tail write fused" if fused else "")
+                       + (", tail write and tile merge fused" if fused else "")
                        + (", early page loads" if kv_ready else ""),
                        "accumulate": "fp32"},
             "tokens_per_s": round(tokens_per_s, 1),

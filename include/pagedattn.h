@@ -197,6 +197,12 @@ int paged_decode_attn_lse_noalloc(const void* q, const void* pool, int64_t pool_
  * by paged_decode_attn_lse on the same stream.  An out-of-range position or
  * page id skips the store and ORs PA_STATUS_BAD_ROW into the workspace status
  * word.  No other call may read or write that pool row while this one runs.
+ *   merged_out, merged_lse  optional (both NULL or both set): device fp32
+ *              [B][n_q_heads][head_dim] (16-byte aligned) and [B][n_q_heads]
+ *              receive the FP32 LSE merge of every request's T tiles, computed
+ *              in the same launch by the CTA that finishes a (request, kv head)
+ *              last, bit-identical to lse_merge over out / lse with
+ *              part_offsets b * T.  With NULL, no merge is done.
  *   flags      0 or PA_DECODE_KV_READY.  The kernels of this library start
  *              under programmatic dependent launch: without the flag a launch
  *              reads nothing in memory until the kernels before it in the
@@ -214,6 +220,7 @@ int paged_decode_attn_lse_append(const void* q, void* pool, int64_t pool_pages,
                                  int n_q_heads, int n_kv_heads, int head_dim,
                                  float scale, const int32_t* positions,
                                  const void* new_rows, float* out, float* lse,
+                                 float* merged_out, float* merged_lse,
                                  void* workspace, size_t workspace_bytes,
                                  unsigned flags, cudaStream_t stream);
 

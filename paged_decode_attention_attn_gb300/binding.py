@@ -219,8 +219,8 @@ def _load():
                                                   i32, ctypes.c_float, vp, vp, vp, vp]
     lib.paged_decode_attn_lse_append.restype = i32
     lib.paged_decode_attn_lse_append.argtypes = [vp, vp, i64, vp, i32, vp, i32, i32, i32, i32,
-                                                 i32, ctypes.c_float, vp, vp, vp, vp, vp, sz,
-                                                 ctypes.c_uint, vp]
+                                                 i32, ctypes.c_float, vp, vp, vp, vp, vp, vp,
+                                                 vp, sz, ctypes.c_uint, vp]
     lib.paged_decode_attn_test_stall.restype = i32
     lib.paged_decode_attn_test_stall.argtypes = [i32, ctypes.c_uint64]
     lib.lse_merge.restype = i32
@@ -408,11 +408,14 @@ def paged_decode_attn_lse_noalloc(q, pool, page_table, tiles, scale, out, lse, s
 
 
 def paged_decode_attn_lse_append(q, pool, page_table, tiles, scale, positions, new_rows, out,
-                                 lse, workspace, stream=None, pool_pages=None, kv_ready=False):
+                                 lse, workspace, stream=None, pool_pages=None, kv_ready=False,
+                                 merged_out=None, merged_lse=None):
     """kv_append_rows and paged_decode_attn_lse in one launch: new_rows bf16
     [B][2*Hkv*D] are stored at token positions int32 [B] (device) of each
     request's pages and attended in place of whatever the pool held there.
-    ``kv_ready`` passes PA_DECODE_KV_READY (see pagedattn.h for the promise)."""
+    ``kv_ready`` passes PA_DECODE_KV_READY (see pagedattn.h for the promise);
+    ``merged_out`` fp32 [B][Hq][D] / ``merged_lse`` [B][Hq] receive the
+    merge of every request's tiles, computed in the same launch."""
     B, Hq, D = q.shape
     row_elems = pool.shape[-1]
     n_kv = row_elems // (2 * D)
@@ -429,7 +432,10 @@ def paged_decode_attn_lse_append(q, pool, page_table, tiles, scale, positions, n
         _dev(page_table, torch.int32, "page_table"), int(page_table.shape[1]), tiles_ptr, B, T,
         Hq, n_kv, D, float(scale), _dev(positions, torch.int32, "positions"),
         _dev(new_rows, torch.bfloat16, "new_rows"), _dev(out, torch.float32, "out"),
-        _dev(lse, torch.float32, "lse"), _dev(workspace, torch.uint8, "workspace"),
+        _dev(lse, torch.float32, "lse"),
+        None if merged_out is None else _dev(merged_out, torch.float32, "merged_out"),
+        None if merged_lse is None else _dev(merged_lse, torch.float32, "merged_lse"),
+        _dev(workspace, torch.uint8, "workspace"),
         workspace.numel(), PA_DECODE_KV_READY if kv_ready else 0, _stream_handle(stream)))
 
 

@@ -45,6 +45,7 @@
 #include <vector>
 
 #include "common.h"
+#include "merge_row.cuh"
 #include "ptx.cuh"
 
 namespace pa {
@@ -104,6 +105,7 @@ struct Params {
   float* lse;
   int32_t* status;
   int32_t* counters;
+  int32_t* req_counters;  // [B][Hkv] tiles finished (fused merge)
   float* part_o;   // [slot][kMaxG][kD]
   float* part_ml;  // [slot][kMaxG][2]
   long long pool_pages;
@@ -132,6 +134,9 @@ struct Params {
   // stage unarmed, so its consumers' wait runs out.
   unsigned long long wait_limit_ns;
   int stall_iteration;
+  // Optional fused cross-tile merge: merged [B][Hq][kD] and [B][Hq].
+  float* m_out;
+  float* m_lse;
   Unit units[kMaxUnits];
 };
 
@@ -185,6 +190,7 @@ struct Shared {
   volatile int* poison;  // [kStages]
   volatile int* abort_flag;
   volatile int* merge_flag;
+  volatile int* fin_flag;
 };
 
 __device__ __forceinline__ Shared carve(uint8_t* raw) {
@@ -200,6 +206,7 @@ __device__ __forceinline__ Shared carve(uint8_t* raw) {
   s.poison = misc;
   s.abort_flag = misc + kStages;
   s.merge_flag = misc + kStages + 1;
+  s.fin_flag = misc + kStages + 2;
   return s;
 }
 
@@ -244,6 +251,35 @@ struct FmaState {
   float m[kMaxG];
   float l[kMaxG];
 };
+
+// Called by every consumer thread once a unit's tile output (request b,
+// tile t, kv head g) is written.  With the fused merge, the CTA that finishes
+// the last tile of (b, g) merges its T tiles for the G query heads of g with
+// the merge kernel's own row routine (same bits as lse_merge over those
+// partials), then resets the counter for the next call.
+template <int kMaxUnits, int kConsumers, int kConsumerWarps>
+__device__ __forceinline__ void finish_unit(const Params<kMaxUnits>& p, const Shared& sh, int b,
+                                            int g, int ct, int warp, int lane) {
+  if (p.m_out == nullptr) return;
+  ptx::named_barrier(1, kConsumers);       // the unit's outputs are all stored
+  if (ct == 0) {
+    __threadfence();
+    const int prev = atomicAdd(p.req_counters + b * p.Hkv + g, 1);
+    *sh.fin_flag = (prev == p.T - 1) ? 1 : 0;
+  }
+  ptx::named_barrier(1, kConsumers);
+  if (*sh.fin_flag) {
+    __threadfence();
+    for (int r = warp; r < p.G; r += kConsumerWarps) {
+      const int h = g * p.G + r;
+      mergerow::merge_row<true>(p.out, p.lse, b * p.T, p.T, p.Hq, h, kD,
+                                p.m_out + ((size_t)b * p.Hq + h) * kD,
+                                p.m_lse + (size_t)b * p.Hq + h, lane);
+    }
+    if (ct == 0) p.req_counters[b * p.Hkv + g] = 0;
+  }
+  ptx::named_barrier(1, kConsumers);
+}
 
 // ---------------------------------------------------------------------------
 // The kernel.
@@ -406,6 +442,7 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       p.out[((size_t)bt * p.Hq + g * G + row) * kD + d] = 0.f;
       if (d == 0) p.lse[(size_t)bt * p.Hq + g * G + row] = -INFINITY;
     }
+    finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, bt / p.T, g, ct, warp, lane);
   }
 
   int it = 0;
@@ -917,7 +954,10 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
           }
         }
         if (ct == 0) p.counters[u] = 0;
+        finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, b, g, ct, warp, lane);
       }
+    } else {
+      finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, b, g, ct, warp, lane);
     }
     ptx::named_barrier(1, kConsumers);
   }
@@ -950,8 +990,14 @@ size_t part_slots(int B, int T, int Hkv) {
   return (size_t)std::min<long long>(units, kMaxUnitsLarge) + kMaxGrid;
 }
 
+// Per (request, kv head) counters of finished tiles for the fused merge.
+size_t request_counter_bytes(int B, int Hkv) {
+  return ((size_t)B * Hkv * 4 + 255) / 256 * 256;
+}
+
 size_t workspace_bytes(int B, int T, int Hkv) {
-  return kStatusBytes + kCounterBytes + part_slots(B, T, Hkv) * (kPartOBytes + kPartMLBytes);
+  return kStatusBytes + kCounterBytes + request_counter_bytes(B, Hkv) +
+         part_slots(B, T, Hkv) * (kPartOBytes + kPartMLBytes);
 }
 
 template <int N, bool TC>
@@ -1004,7 +1050,7 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
         int n_q_heads, int n_kv_heads, int head_dim, float scale, float* out, float* lse,
         void* workspace, size_t ws_bytes, cudaStream_t stream,
         const int32_t* positions = nullptr, const void* new_rows = nullptr,
-        unsigned flags = 0) {
+        unsigned flags = 0, float* merged_out = nullptr, float* merged_lse = nullptr) {
   clear_error();
   PA_REQUIRE(B >= 0 && T >= 0, "B and T must be >= 0 (got %d, %d)", B, T);
   if ((long long)B * T == 0) return PA_OK;
@@ -1037,6 +1083,10 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
                max_tok);
   }
   PA_REQUIRE((flags & ~PA_DECODE_KV_READY) == 0, "unknown flags %#x", flags);
+  PA_REQUIRE((merged_out == nullptr) == (merged_lse == nullptr),
+             "merged_out and merged_lse go together");
+  PA_REQUIRE(merged_out == nullptr || reinterpret_cast<uintptr_t>(merged_out) % 16 == 0,
+             "merged_out must be 16-byte aligned");
   PA_REQUIRE((positions == nullptr) == (new_rows == nullptr),
              "positions and new_rows go together");
   PA_REQUIRE(new_rows == nullptr || reinterpret_cast<uintptr_t>(new_rows) % 16 == 0,
@@ -1086,8 +1136,11 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
   common.status = reinterpret_cast<int32_t*>(ws);
   common.counters = reinterpret_cast<int32_t*>(ws + kStatusBytes);
   const size_t slots = part_slots(B, T, n_kv_heads);
-  common.part_o = reinterpret_cast<float*>(ws + kStatusBytes + kCounterBytes);
-  common.part_ml = reinterpret_cast<float*>(ws + kStatusBytes + kCounterBytes + slots * kPartOBytes);
+  const size_t rc_bytes = request_counter_bytes(B, n_kv_heads);
+  common.req_counters = reinterpret_cast<int32_t*>(ws + kStatusBytes + kCounterBytes);
+  common.part_o = reinterpret_cast<float*>(ws + kStatusBytes + kCounterBytes + rc_bytes);
+  common.part_ml = reinterpret_cast<float*>(ws + kStatusBytes + kCounterBytes + rc_bytes +
+                                            slots * kPartOBytes);
   common.pool_pages = pool_pages;
   common.max_pages = max_pages;
   common.T = T;
@@ -1100,6 +1153,8 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
   common.positions = positions;
   common.row_elems = row_elems;
   common.kv_ready = (flags & PA_DECODE_KV_READY) ? 1 : 0;
+  common.m_out = merged_out;
+  common.m_lse = merged_lse;
   common.wait_limit_ns = t_wait_limit_ns ? t_wait_limit_ns : kWaitLimitNs;
   common.stall_iteration = t_stall_iteration;
   t_stall_iteration = -1;
@@ -1187,7 +1242,8 @@ extern "C" int paged_decode_attn_lse_append(const void* q, void* pool, int64_t p
                                             const int32_t* tiles, int B, int T, int n_q_heads,
                                             int n_kv_heads, int head_dim, float scale,
                                             const int32_t* positions, const void* new_rows,
-                                            float* out, float* lse, void* workspace,
+                                            float* out, float* lse, float* merged_out,
+                                            float* merged_lse, void* workspace,
                                             size_t workspace_bytes, unsigned flags,
                                             cudaStream_t stream) {
   pa::clear_error();
@@ -1195,7 +1251,8 @@ extern "C" int paged_decode_attn_lse_append(const void* q, void* pool, int64_t p
     return pa::fail(PA_ERR_INVALID, "positions and new_rows are required");
   return pa::decode::run(true, q, pool, pool_pages, page_table, max_pages, tiles, B, T,
                          n_q_heads, n_kv_heads, head_dim, scale, out, lse, workspace,
-                         workspace_bytes, stream, positions, new_rows, flags);
+                         workspace_bytes, stream, positions, new_rows, flags, merged_out,
+                         merged_lse);
 }
 
 extern "C" int paged_decode_attn_lse_cuda_core(const void* q, const void* pool,

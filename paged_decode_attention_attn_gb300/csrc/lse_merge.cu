@@ -13,13 +13,13 @@
 #include <cmath>
 
 #include "common.h"
+#include "merge_row.cuh"
 #include "ptx.cuh"
 
 namespace pa {
 namespace merge {
 
 constexpr int kWarpsPerBlock = 8;
-constexpr int kVecPerLane = 2;  // float4 chunks of the output row per lane per pass
 
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     lse_merge_kernel(const float* __restrict__ out_parts, const float* __restrict__ lse_parts,
@@ -34,62 +34,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int h = static_cast<int>(wid - (long long)b * H);
   const int p0 = offsets[b];
   const int n = offsets[b + 1] - p0;
-  float* orow = out + ((size_t)b * H + h) * D;
-
-  float big_m = -INFINITY;
-  int nan = 0;
-  for (int i = lane; i < n; i += 32) {
-    const float x = lse_parts[(size_t)(p0 + i) * H + h];
-    nan |= (x != x);
-    big_m = fmaxf(big_m, x);
-  }
-#pragma unroll
-  for (int off = 16; off >= 1; off >>= 1) {
-    big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, off));
-    nan |= __shfl_xor_sync(0xffffffffu, nan, off);
-  }
-  const int n4 = D / 4;
-  if (nan || n <= 0 || big_m == -INFINITY) {
-    const float fill = nan ? __int_as_float(0x7fc00000) : 0.f;
-    for (int c = lane; c < n4; c += 32)
-      reinterpret_cast<float4*>(orow)[c] = make_float4(fill, fill, fill, fill);
-    if (lane == 0) lse[(size_t)b * H + h] = nan ? fill : -INFINITY;
-    return;
-  }
-  float wsum = 0.f;
-  for (int c0 = 0; c0 < n4; c0 += 32 * kVecPerLane) {
-    float4 acc[kVecPerLane];
-#pragma unroll
-    for (int v = 0; v < kVecPerLane; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
-    float ws = 0.f;
-    for (int i = 0; i < n; ++i) {
-      const float w = expf(lse_parts[(size_t)(p0 + i) * H + h] - big_m);
-      ws += w;
-      const float4* src =
-          reinterpret_cast<const float4*>(out_parts + ((size_t)(p0 + i) * H + h) * D);
-#pragma unroll
-      for (int v = 0; v < kVecPerLane; ++v) {
-        const int c = c0 + v * 32 + lane;
-        if (c < n4) {
-          const float4 x = src[c];
-          acc[v].x = fmaf(w, x.x, acc[v].x);
-          acc[v].y = fmaf(w, x.y, acc[v].y);
-          acc[v].z = fmaf(w, x.z, acc[v].z);
-          acc[v].w = fmaf(w, x.w, acc[v].w);
-        }
-      }
-    }
-#pragma unroll
-    for (int v = 0; v < kVecPerLane; ++v) {
-      const int c = c0 + v * 32 + lane;
-      if (c < n4)
-        reinterpret_cast<float4*>(orow)[c] =
-            make_float4(acc[v].x / ws, acc[v].y / ws, acc[v].z / ws, acc[v].w / ws);
-    }
-    wsum = ws;
-  }
-  if (lane == 0) lse[(size_t)b * H + h] =
-        static_cast<float>(static_cast<double>(big_m) + log(static_cast<double>(wsum)));
+  mergerow::merge_row<false>(out_parts, lse_parts, p0, n, H, h, D,
+                             out + ((size_t)b * H + h) * D, lse + (size_t)b * H + h, lane);
 }
 
 // One warp per row: copy rows[b] into the pool row of token positions[b].

@@ -1,0 +1,100 @@
+// The FP32 log-sum-exp merge of one (request, head) row, shared by the merge
+// kernel and the decode kernel's fused cross-tile merge so that both give the
+// same bits.
+//
+// Merge rule ("KV-cache engineering", section "Exact recent pages, compact
+// older pages"): weight each partial by exp(LSE_i - max LSE), sum the weighted
+// outputs, divide by the summed weights, and return max + log(sum) as the
+// merged LSE.  One warp per row; partials are read in increasing order so the
+// result is deterministic, and the division by the summed weights (not a
+// multiply by its reciprocal) returns a single partial bit for bit.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cmath>
+
+namespace pa {
+namespace mergerow {
+
+constexpr int kVecPerLane = 2;  // float4 chunks of the output row per lane per pass
+
+// kL2: read through L2 only (partials written by other CTAs of the running
+// kernel); otherwise plain loads (partials from an earlier kernel).
+template <bool kL2>
+__device__ __forceinline__ float load1(const float* p) {
+  if constexpr (kL2) return __ldcg(p);
+  else return *p;
+}
+template <bool kL2>
+__device__ __forceinline__ float4 load4(const float4* p) {
+  if constexpr (kL2) return __ldcg(p);
+  else return *p;
+}
+
+// Partial i of the row is out_parts[((p0 + i) * H + h) * D ...] with LSE
+// lse_parts[(p0 + i) * H + h], i < n.  Writes orow[0..D) and *lse_out.  D is
+// a multiple of 4 and the rows 16-byte aligned.  Called by all 32 lanes.
+template <bool kL2>
+__device__ __forceinline__ void merge_row(const float* out_parts, const float* lse_parts, int p0, int n, int H,
+                          int h, int D, float* orow, float* lse_out, int lane) {
+  float big_m = -INFINITY;
+  int nan = 0;
+  for (int i = lane; i < n; i += 32) {
+    const float x = load1<kL2>(lse_parts + (size_t)(p0 + i) * H + h);
+    nan |= (x != x);
+    big_m = fmaxf(big_m, x);
+  }
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, off));
+    nan |= __shfl_xor_sync(0xffffffffu, nan, off);
+  }
+  const int n4 = D / 4;
+  if (nan || n <= 0 || big_m == -INFINITY) {
+    const float fill = nan ? __int_as_float(0x7fc00000) : 0.f;
+    for (int c = lane; c < n4; c += 32)
+      reinterpret_cast<float4*>(orow)[c] = make_float4(fill, fill, fill, fill);
+    if (lane == 0) *lse_out = nan ? fill : -INFINITY;
+    return;
+  }
+  float wsum = 0.f;
+  for (int c0 = 0; c0 < n4; c0 += 32 * kVecPerLane) {
+    float4 acc[kVecPerLane];
+#pragma unroll
+    for (int v = 0; v < kVecPerLane; ++v) acc[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ws = 0.f;
+    // (Issuing a batch of partials' loads before their arithmetic measured
+    // slower inside the decode kernel.)
+    for (int i = 0; i < n; ++i) {
+      const float w = expf(load1<kL2>(lse_parts + (size_t)(p0 + i) * H + h) - big_m);
+      ws += w;
+      const float4* src =
+          reinterpret_cast<const float4*>(out_parts + ((size_t)(p0 + i) * H + h) * D);
+#pragma unroll
+      for (int v = 0; v < kVecPerLane; ++v) {
+        const int c = c0 + v * 32 + lane;
+        if (c < n4) {
+          const float4 x = load4<kL2>(src + c);
+          acc[v].x = fmaf(w, x.x, acc[v].x);
+          acc[v].y = fmaf(w, x.y, acc[v].y);
+          acc[v].z = fmaf(w, x.z, acc[v].z);
+          acc[v].w = fmaf(w, x.w, acc[v].w);
+        }
+      }
+    }
+#pragma unroll
+    for (int v = 0; v < kVecPerLane; ++v) {
+      const int c = c0 + v * 32 + lane;
+      if (c < n4)
+        reinterpret_cast<float4*>(orow)[c] =
+            make_float4(acc[v].x / ws, acc[v].y / ws, acc[v].z / ws, acc[v].w / ws);
+    }
+    wsum = ws;
+  }
+  if (lane == 0)
+    *lse_out = static_cast<float>(static_cast<double>(big_m) + log(static_cast<double>(wsum)));
+}
+
+}  // namespace mergerow
+}  // namespace pa

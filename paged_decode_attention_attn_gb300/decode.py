@@ -1,9 +1,10 @@
 """One decode step of paged GQA attention over every layer, on two routes.
 
 Resident route: the whole history sits in a device pool; per layer one
-launch writes the new token's row into its page and returns per-tile (out,
-LSE) with that row attended (``fused=False`` issues the tail write and the
-attention as two launches), and the FP32 merge combines the tiles.
+launch writes the new token's row into its page, returns per-tile (out, LSE)
+with that row attended and merges every request's tiles in FP32
+(``fused=False`` issues the tail write, the attention and the merge as three
+launches).
 
 Staged route ("Staging without a stall"; "KV-cache engineering", section
 "Staging layers under a lease"): pinned host memory owns the history; per
@@ -27,18 +28,20 @@ from .workloads import DecodeWorkload, history_rows
 
 def _layer_kernels(fused, cuda_core, q, pool, table, positions, new_row, tiles, scale, tile_out,
                    tile_lse, workspace, status, part_offsets, out, lse, stream, kv_ready=False):
-    """The layer's kernels: tail write + attention (one fused launch, or two),
-    then the merge of the tiles."""
+    """The layer's kernels: tail write + attention + merge of the tiles in one
+    launch (fused), or as three launches."""
     geo_h, geo_d = tile_out.shape[-2], tile_out.shape[-1]
     n_tiles = np.asarray(tiles).shape[1]
     if fused and not cuda_core:
+        merged = n_tiles > 1
         B.paged_decode_attn_lse_append(q, pool, table, tiles, scale, positions, new_row,
                                        tile_out, tile_lse, workspace, stream=stream,
-                                       kv_ready=kv_ready)
-    else:
-        B.kv_append_rows(pool, table, positions, new_row, status=status, stream=stream)
-        B.paged_decode_attn_lse(q, pool, table, tiles, scale, tile_out, tile_lse, workspace,
-                                stream=stream, cuda_core=cuda_core)
+                                       kv_ready=kv_ready, merged_out=out if merged else None,
+                                       merged_lse=lse if merged else None)
+        return
+    B.kv_append_rows(pool, table, positions, new_row, status=status, stream=stream)
+    B.paged_decode_attn_lse(q, pool, table, tiles, scale, tile_out, tile_lse, workspace,
+                            stream=stream, cuda_core=cuda_core)
     if n_tiles > 1:
         # With one tile per request the merge is the identity (a single
         # partial is returned bit for bit): out and lse are views of the tile

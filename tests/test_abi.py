@@ -96,16 +96,18 @@ def test_fused_append_argument_checks(B):
     fake = 1 << 20
     arr = np.ascontiguousarray(np.asarray([[[0, 64]]], dtype=np.int32))
 
-    def call(positions, rows, flags=0):
+    def call(positions, rows, flags=0, merged=None):
         return B.lib.paged_decode_attn_lse_append(fake, fake, 16, fake, 8, arr.ctypes.data, 1, 1,
                                                   24, 4, 256, 0.0625, positions, rows, fake, fake,
-                                                  fake, 1 << 30, flags, None)
+                                                  merged, merged, fake, 1 << 30, flags, None)
     assert call(None, fake) == B.PA_ERR_INVALID
     assert call(fake, None) == B.PA_ERR_INVALID
     assert call(fake, fake + 8) == B.PA_ERR_INVALID
     assert "new_rows" in B.last_error()
     assert call(fake, fake, flags=2) == B.PA_ERR_INVALID
     assert "flags" in B.last_error()
+    assert call(fake, fake, merged=fake + 4) == B.PA_ERR_INVALID
+    assert "merged_out" in B.last_error()
 
 
 def test_stall_hook_argument_checks(B):

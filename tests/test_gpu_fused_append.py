@@ -152,3 +152,30 @@ def test_early_page_loads_change_no_bits(D, make):
         runs.append((dec, tc))
     (a, ta), (b, tb) = runs
     assert_same(a, b, ta, tb)
+
+
+def test_fused_merge_many_tiles_and_repeated_steps(D):
+    # up to 20 tiles per request (some empty, some overlapping, one request
+    # with a single tile): the in-kernel merge equals lse_merge bit for bit on
+    # every one of three consecutive steps (its counters reset each time).
+    rng = np.random.default_rng(12)
+    lengths = [3000, 700, 64, 5000]
+    tiles = []
+    for L in lengths:
+        cuts = sorted(rng.integers(0, L, size=18).tolist())
+        t_req = [(0, cuts[0])] + [(a, b) for a, b in zip(cuts, cuts[1:])] + [(cuts[-1], L)]
+        tiles.append(t_req[:20])
+    tiles[2] = [(0, 64)]
+    w = wl.custom(lengths, tiles, seed=17, n_spare=4, n_layers=2)
+    t = wl.materialize(w, "cuda")
+    poison_new_rows(w, t)
+    tf, tu = clone(t), clone(t)
+    fused = D.ResidentDecode(w, tf, fused=True)
+    unfused = D.ResidentDecode(w, tu, fused=False)
+    torch.cuda.synchronize()
+    for _ in range(3):
+        fused.step()
+        unfused.step()
+        torch.cuda.synchronize()
+        assert fused.kernel_status() == 0 and unfused.kernel_status() == 0
+        assert_same(fused, unfused, tf, tu)
