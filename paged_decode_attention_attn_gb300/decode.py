@@ -1,4 +1,4 @@
-"""One decode step of paged GQA attention over every layer, on two routes.
+"""One decode step of paged GQA attention over every layer, on three routes.
 
 Resident route: the whole history sits in a device pool; per layer one
 launch writes the new token's row into its page, returns per-tile (out, LSE)
@@ -13,8 +13,16 @@ the H2D stream, the compute stream waits on the copy's event, the same
 kernels run against the slot, attention is marked done, and only the new
 token's row is written back to its pinned host row on the D2H stream.
 
-Both routes only sequence C-ABI calls; all data movement and arithmetic run in
-libpagedattn's kernels and copies.
+Planned route ("Staging without a stall", section "Admission that does
+arithmetic"): the admission planner decides each step which pages stay hot in
+a device pool; pages that turn hot are copied in once, the rest are staged.
+
+On the staged and planned routes, pages the background converter has
+published ("KV-cache engineering", section "Exact recent pages, compact older
+pages") can be staged in their compact form (``CompactStore``).
+
+The routes only sequence C-ABI calls; all data movement and arithmetic run in
+libpagedattn's kernels, copies and threads.
 """
 
 from __future__ import annotations
