@@ -404,13 +404,19 @@ def run_ours(args):
     null_ms = null_arm(args, w, t, D, B, dev, fused, kv_ready)
 
     # ---- staged route, end to end through host buffers ----
-    e2e = e2e_compact = None
+    e2e = e2e_compact = e2e_tiled = None
     if not args.no_e2e:
         e2e = run_e2e(args, w, t, dev, D, B)
         # whole job: every rank's bytes over the slowest rank's wall time
         secs = max_over_ranks(e2e.pop("_secs"), world)
         e2e["value"] = round(whole_job_gbs(kv_bytes, e2e["steps"], secs * 1e3, world), 2)
         e2e["ms_per_step"] = round(1e3 * secs / e2e["steps"], 3)
+        if not w.window:
+            e2e_tiled = run_e2e(args, w, t, dev, D, B, tiled=True)
+            secs = max_over_ranks(e2e_tiled.pop("_secs"), world)
+            e2e_tiled["value"] = round(whole_job_gbs(kv_bytes, e2e_tiled["steps"], secs * 1e3,
+                                                     world), 2)
+            e2e_tiled["ms_per_step"] = round(1e3 * secs / e2e_tiled["steps"], 3)
         if not args.no_compact:
             e2e_compact = run_e2e(args, w, t, dev, D, B, compact=True,
                                   exact=(res.o.out, res.o.lse))
@@ -464,6 +470,8 @@ def run_ours(args):
             line["e2e"] = e2e
         if e2e_compact is not None:
             line["e2e_compact"] = e2e_compact
+        if e2e_tiled is not None:
+            line["e2e_tiled"] = e2e_tiled
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
@@ -524,7 +532,7 @@ def null_arm(args, w, t, D, B, dev, fused, kv_ready):
     return e0.elapsed_time(e1) / n
 
 
-def run_e2e(args, w, t, dev, D, B, compact=False, exact=None):
+def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
     """Staged route: host-owned history, host Q / new rows in, outputs out.
 
     compact=True: every page below the new token is first converted by the
@@ -543,7 +551,10 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None):
         store.mark_written(w.lengths)
         store.compactor.wait_idle()
         convert_s = time.perf_counter() - c0
-    st = D.StagedDecode(w, t, host, n_slots=2, compute_stream=compute, compact=store)
+    if tiled:       # staged per (request, tile) into two tile slots
+        st = D.TiledStagedDecode(w, t, host, n_slots=2, compute_stream=compute)
+    else:
+        st = D.StagedDecode(w, t, host, n_slots=2, compute_stream=compute, compact=store)
     q_host = t["q"].cpu().pin_memory()
     rows_host = t["new_rows"].cpu().pin_memory()
     out_host = torch.empty(st.o.out.shape, dtype=torch.float32).pin_memory()
@@ -588,7 +599,7 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None):
     if st.kernel_status() != 0:
         raise RuntimeError("staged route kernel status non-zero")
     stats = st.handle.stats()
-    staged_per_step = stats.staged_bytes // stats.stage_generation * w.n_layers
+    staged_per_step = stats.staged_bytes // stats.stage_generation * st.stages_per_step()
     probe_after = link_probe()
     del dst
     h2d = q_host.numel() * 2 + rows_host.numel() * 2 + staged_per_step
@@ -596,8 +607,10 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None):
     kv = w.kv_bytes_per_step()
     res = {"value": round(kv * steps / secs / 1e9, 2), "unit": UNIT,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-           "route": "host-staged, 2 arena slots, tail write-back"
+           "route": ("host-staged per tile, 2 tile slots" if tiled
+                     else "host-staged, 2 arena slots") + ", tail write-back"
                     + (", published pages staged compact" if compact else ""),
+           "arena_bytes": int(st.arena_bytes()),
            "ms_per_step": round(1e3 * secs / steps, 3),
            "h2d_GBps": round(staged_per_step * steps / secs / 1e9, 2),
            "link_probe_h2d_GBps": [round(probe_before, 2), round(probe_after, 2)],

@@ -367,6 +367,12 @@ class StagedDecode:
             plan.append(out)
         self.plan = plan
 
+    def arena_bytes(self) -> int:
+        return self.arena_buf.numel()
+
+    def stages_per_step(self) -> int:
+        return self.n_layers
+
     def staged_bytes_per_step(self) -> int:
         """Host-to-device bytes the current plan moves per step."""
         geo = self.w.geometry
@@ -423,6 +429,135 @@ class StagedDecode:
 
     def close(self):
         self.handle.close()
+
+
+def tile_units(w: DecodeWorkload):
+    """(request, tile index, start, end) of every tile, in request then tile
+    order (empty tiles included: their launch writes output 0, LSE -inf)."""
+    return [(r, k, int(w.tiles[r, k, 0]), int(w.tiles[r, k, 1]))
+            for r in range(w.batch) for k in range(w.n_tiles)]
+
+
+def tile_kernels(w, t, i, r, k, s, e, pool, table_row, o, workspace, stream):
+    """Attention of one (request, tile) as its own launch (B = 1): fused with
+    the new row's store and substitution when the tile holds the new token."""
+    geo = w.geometry
+    tiles = np.array([[[s, e]]], dtype=np.int32)
+    out = o.tile_out[i][r:r + 1, k:k + 1]
+    lse = o.tile_lse[i][r:r + 1, k:k + 1]
+    L = int(w.lengths[r])
+    if s <= L - 1 < e:
+        B.paged_decode_attn_lse_append(t["q"][i][r:r + 1], pool, table_row, tiles, geo.scale,
+                                       t["positions"][r:r + 1], t["new_rows"][i][r:r + 1], out,
+                                       lse, workspace, stream=stream)
+    else:
+        B.paged_decode_attn_lse(t["q"][i][r:r + 1], pool, table_row, tiles, geo.scale, out, lse,
+                                workspace, stream=stream)
+
+
+class TiledStagedDecode:
+    """Host-owned history staged per (request, tile) instead of per layer: the
+    arena holds ``n_slots`` slots of one tile's pages ("GPU memory
+    management", section "Pages held by right, borrowed or free": the arena
+    stages pages for 32K-token tiles), each tile is attended by its own launch
+    as soon as its
+    copy lands, and the layer's tiles are merged after the last one.  The
+    device working set is n_slots tiles whatever the context length.
+
+    Results equal, bit for bit, the resident route run with the same launches
+    (one per tile; ``resident_tiled_step``); a launch's split points depend on
+    its own pages, so they differ from the one-launch-per-layer route at the
+    rounding level.  Workloads with a resident window are not supported here.
+    """
+
+    def __init__(self, w: DecodeWorkload, t: dict, host: HostHistory, n_slots: int = 2,
+                 compute_stream=None):
+        if w.window:
+            raise ValueError("TiledStagedDecode stages whole tiles; no resident window")
+        geo = w.geometry
+        pt = geo.page_tokens
+        self.w, self.t, self.host = w, t, host
+        self.n_layers = t["pool"].shape[0]
+        dev = t["pool"].device
+        self.compute = compute_stream or torch.cuda.current_stream(dev)
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.units = tile_units(w)
+        self.slot_pages = max([-(-e // pt) - s // pt for _, _, s, e in self.units if e > s],
+                              default=1)
+        self.arena = torch.full((n_slots * self.slot_pages, pt, geo.row_elems), float("nan"),
+                                dtype=torch.bfloat16, device=dev)
+        self.page_tables = torch.zeros((n_slots, w.batch, w.max_pages), dtype=torch.int32,
+                                       device=dev)
+        torch.cuda.synchronize(dev)
+        self.handle = B.Arena(self.arena.data_ptr(), self.arena.numel() * 2, geo.row_bytes,
+                              n_slots, 0, self.slot_pages, self.page_tables.data_ptr(),
+                              w.batch, w.max_pages, compute_stream=self.compute,
+                              h2d_stream=self.h2d, d2h_stream=self.d2h)
+        self.o = _Outputs(w, self.n_layers, dev)
+        self.workspace = B.alloc_workspace(1, 1, geo.n_q_heads, geo.n_kv_heads, geo.head_dim,
+                                           device=dev)
+
+    def arena_bytes(self) -> int:
+        return self.arena.numel() * 2
+
+    def stages_per_step(self) -> int:
+        return self.n_layers * sum(1 for _, _, s, e in self.units if e > s)
+
+    def layer(self, i: int):
+        w, geo = self.w, self.w.geometry
+        pt = geo.page_tokens
+        for u, (r, k, s, e) in enumerate(self.units):
+            if e <= s:           # nothing to stage: the launch writes 0 / -inf
+                tile_kernels(w, self.t, i, r, k, s, e, self.arena, self.page_tables[0][r:r + 1],
+                             self.o, self.workspace, self.compute)
+                continue
+            L = int(w.lengths[r])
+            p0, p1 = s // pt, -(-e // pt)
+            rows = min(p1 * pt, L - 1) - p0 * pt
+            owner = (i << 32) | r
+            key = i * len(self.units) + u
+            slot, _ = self.handle.stage_layer(key, [(r, owner, [dict(
+                logical_page=p0, n_pages=p1 - p0, n_rows=max(0, rows),
+                host_rows=self.host.row_address(i, r, p0 * pt))])])
+            tile_kernels(w, self.t, i, r, k, s, e, self.arena,
+                         self.page_tables[slot][r:r + 1], self.o, self.workspace, self.compute)
+            self.handle.mark_attention_done(key)
+            if s <= L - 1 < e:
+                self.handle.writeback_tail(key, [(r, L - 1, self.host.row_address(i, r, L - 1),
+                                                  owner)])
+        if w.n_tiles > 1:
+            o = self.o
+            B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
+                        o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
+                        o.lse[i], stream=self.compute)
+
+    def step(self):
+        for i in range(self.n_layers):
+            self.layer(i)
+
+    def drain(self):
+        self.handle.drain()
+
+    def kernel_status(self) -> int:
+        return int(self.workspace[:4].view(torch.int32).item())
+
+    def close(self):
+        self.handle.close()
+
+
+def resident_tiled_step(w, t, o, workspace, stream=None):
+    """The resident route with TiledStagedDecode's launches: one attention
+    launch per (request, tile) over the device pool, then the tile merge."""
+    geo = w.geometry
+    for i in range(t["pool"].shape[0]):
+        for r, k, s, e in tile_units(w):
+            tile_kernels(w, t, i, r, k, s, e, t["pool"][i], t["page_table"][r:r + 1], o,
+                         workspace, stream)
+        if w.n_tiles > 1:
+            B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),
+                        o.tile_lse[i].view(-1, geo.n_q_heads), o.part_offsets, o.out[i],
+                        o.lse[i], stream=stream)
 
 
 class PlannedDecode:

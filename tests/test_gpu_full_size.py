@@ -114,3 +114,47 @@ def test_staged_route_is_bit_identical_to_resident(D, name, n_slots, leases):
     host.close()
     del staged, res, host, t
     _free()
+
+
+@pytest.mark.parametrize("make", [lambda: wl.one_request_262144(n_layers=2),
+                                  lambda: wl.four_requests_31744(n_layers=2),
+                                  lambda: wl.custom([5000, 70000], [[(0, 2000), (2000, 5000)],
+                                                                   [(0, 32768), (32768, 65536),
+                                                                    (65536, 70000)]],
+                                                    seed=19, n_layers=2)],
+                         ids=["1x262144", "4x31744", "uneven-tiles"])
+def test_tile_staged_route_is_bit_identical_to_resident_tile_launches(D, make):
+    """Staging per 32K-token tile into two tile slots gives the bits of the
+    resident route with the same per-tile launches, writes every new row back
+    exactly, and keeps the arena at two tiles."""
+    w = make()
+    t = wl.materialize(w, "cuda")
+    host = D.HostHistory(w, t)
+    staged = D.TiledStagedDecode(w, t, host, n_slots=2)
+    staged.step()
+    staged.drain()
+    torch.cuda.synchronize()
+    ref = D._Outputs(w, w.n_layers, "cuda")
+    geo = w.geometry
+    ws = D.B.alloc_workspace(1, 1, geo.n_q_heads, geo.n_kv_heads, geo.head_dim)
+    D.resident_tiled_step(w, t, ref, ws)
+    torch.cuda.synchronize()
+    assert int(staged.workspace[:4].view(torch.int32).item()) == 0
+    assert int(ws[:4].view(torch.int32).item()) == 0
+    assert torch.equal(staged.o.tile_out, ref.tile_out)
+    assert torch.equal(staged.o.tile_lse, ref.tile_lse)
+    assert torch.equal(staged.o.out, ref.out) and torch.equal(staged.o.lse, ref.lse)
+    for i in range(w.n_layers):
+        for r in range(w.batch):
+            row = host.row(i, r, int(w.lengths[r]) - 1)
+            assert torch.equal(row.view(torch.int16), t["new_rows"][i, r].cpu().view(torch.int16))
+    # and the tiled results agree with the one-launch-per-layer route to rounding
+    res = D.ResidentDecode(w, t)
+    res.step()
+    torch.cuda.synchronize()
+    assert max_abs(staged.o.out.cpu(), res.o.out.cpu()) <= TOL_SPLIT
+    assert staged.arena_bytes() <= 2 * 512 * 64 * geo.row_bytes     # two 32K-token tiles
+    staged.close()
+    host.close()
+    del staged, host, t, res
+    _free()
