@@ -97,9 +97,11 @@ const char* pa_version(void);
 /* Decode attention with per-tile LSE  ([KVE-exact], [KVE-bus])             */
 /* ------------------------------------------------------------------------ */
 
-/* Workspace bytes paged_decode_attn_lse / paged_decode_attn_lse_cuda_core
- * need for B requests x T tiles of this geometry (an upper bound that does not
- * depend on tile contents).  Returns 0 for an unsupported geometry. */
+/* Workspace bytes paged_decode_attn_lse, paged_decode_attn_lse_cuda_core and
+ * paged_decode_attn_lse_append need for B requests x T tiles of this geometry
+ * (an upper bound that does not depend on tile contents): status word, split
+ * counters, per-(request, kv head) tile counters, partial slots.  Returns 0
+ * for an unsupported geometry. */
 size_t paged_decode_attn_lse_workspace_bytes(int B, int T, int n_q_heads,
                                              int n_kv_heads, int head_dim);
 
