@@ -1,7 +1,9 @@
 /*
  * pagedattn.h -- C ABI of libpagedattn: paged GQA decode attention with a
- * per-tile log-sum-exp, an FP32 LSE merge, and a staging arena that moves a
- * layer's KV history from pinned host memory into bounded device slots.
+ * per-tile log-sum-exp, an FP32 LSE merge, a staging arena that moves KV
+ * history from pinned host memory into bounded device slots (stage calls or
+ * leases), an admission planner for a device pool, and a background converter
+ * of fully written pages into a compact representation.
  *
  * Sources (web pages, cited by title and section):
  *   [KVE-exact]  "KV-cache engineering", section "Exact recent pages, compact
@@ -30,13 +32,18 @@
  *   [GMM-host]   "GPU memory management", section "A host pool that explains
  *                its own size": a history is, per layer, a segment of
  *                context length x 4,096 bytes.
+ *   [KVE-tier]   "KV-cache engineering", section "What the hybrid tier buys":
+ *                a representation is judged by the bytes per token it stops
+ *                moving over the bus.
  *
  * Conventions for every entry point:
  *   - All memory is allocated and owned by the caller.  The library keeps raw
  *     pointers only for the lifetime the call documents and never frees them.
  *   - Streams are the caller's.  Kernels and copies are enqueued
- *     asynchronously; no entry point synchronises the host except
- *     kv_arena_drain.
+ *     asynchronously; no entry point waits for the device except
+ *     kv_arena_drain and kv_lease_retire (documented host waits);
+ *     kv_compactor_wait_idle and kv_compactor_destroy wait for the library's
+ *     converter threads, never for the device.
  *   - Return value: PA_OK (0) or a negative PA_ERR_* code; a thread-local
  *     message is available from kv_last_error().  No C++ exception crosses
  *     the ABI.
