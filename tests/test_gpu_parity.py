@@ -240,3 +240,31 @@ def test_lse_merge_identity_and_edges(B):
     assert torch.equal(out[3], parts5[2]) and torch.equal(lse[3], lses5[2])
     assert torch.isnan(lse[4, 5]) and torch.isnan(out[4, 5]).all()
     assert torch.isfinite(out[4, :5]).all()
+
+
+GEOMETRIES = [(8, 8), (8, 1), (32, 4), (16, 2), (12, 6), (7, 7)]
+
+
+@pytest.mark.parametrize("hq,hkv", GEOMETRIES, ids=[f"{a}q{b}kv" for a, b in GEOMETRIES])
+def test_other_head_geometries_match_oracle(B, D, hq, hkv):
+    # group sizes 1..8 and kv-head counts 1..8: every request's tiles and the
+    # fused tail write and merge against the oracle, and the fused route
+    # against the three-launch route bit for bit
+    geo = wl.Geometry(n_q_heads=hq, n_kv_heads=hkv)
+    w = wl.custom([700, 3000, 65], [[(0, 700), (100, 350)], [(0, 1500), (1500, 3000)],
+                                     [(0, 65), (64, 65)]], seed=33, n_spare=3, geometry=geo)
+    t = wl.materialize(w, "cuda")
+    fused = D.ResidentDecode(w, {k: v.clone() for k, v in t.items()}, fused=True)
+    split = D.ResidentDecode(w, {k: v.clone() for k, v in t.items()}, fused=False)
+    torch.cuda.synchronize()
+    fused.step()
+    split.step()
+    torch.cuda.synchronize()
+    assert fused.kernel_status() == 0 and split.kernel_status() == 0
+    assert torch.equal(fused.o.out, split.o.out) and torch.equal(fused.o.lse, split.o.lse)
+    assert torch.equal(fused.o.tile_out, split.o.tile_out)
+    for r in range(w.batch):
+        ref = oracle_request(w, t, 0, r)
+        o = fused.o
+        assert_close_to_oracle(o.tile_out[0, r], o.tile_lse[0, r], o.out[0, r], o.lse[0, r],
+                               ref, w.tiles[r], f"{hq}q/{hkv}kv request {r}")
