@@ -43,7 +43,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_kernel_4x31744.md")
 KERNEL_SOURCE = os.path.join(ROOT, "paged_decode_attention_attn_gb300", "csrc", "decode_attn.cu")
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
@@ -58,7 +58,8 @@ def parse_args():
     ap.add_argument("--cuda-core", action="store_true",
                     help="time the CUDA-core attention kernel instead of the tensor-core one")
     ap.add_argument("--unfused", action="store_true",
-                    help="issue the tail write and the attention as two launches per layer")
+                    help="issue the tail write, the attention and the merge as separate "
+                         "launches per layer")
     ap.add_argument("--no-early-kv", action="store_true",
                     help="make each launch wait for the previous kernel before loading pages")
     ap.add_argument("--no-e2e", action="store_true")
@@ -69,7 +70,7 @@ def parse_args():
     ap.add_argument("--bus-model", action="store_true",
                     help="fit the staged route's latency model over 32K-262K tokens "
                          "(prints its own JSON line instead of the bench line)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 # ---------------------------------------------------------------------------
