@@ -78,7 +78,8 @@ constexpr size_t kStatusBytes = 256;
 constexpr size_t kCounterBytes = 4 * kMaxUnitsLarge;
 constexpr size_t kPartOBytes = size_t(kMaxG) * kD * 4;   // per partial slot
 constexpr size_t kPartMLBytes = size_t(kMaxG) * 2 * 4;
-constexpr double kLn2 = 0.693147180559945309;
+constexpr float kLn2Hi = 0.693145751953125f;        // ln 2, high bits (exact products)
+constexpr float kLn2Lo = 1.428606765330187045e-06f; // ln 2 - kLn2Hi
 constexpr float kLog2e = 1.44269504088896341f;
 // The running softmax reference is kept on multiples of kRefStep (log2 units):
 // rescales and the weights between partials are then exact powers of two, and
@@ -165,10 +166,18 @@ __device__ __forceinline__ int first_unit(const Params<N>& p, long long start) {
 }
 
 // ln-domain LSE of a reference m (log2 units, a multiple of kRefStep) and a
-// sum l: m ln 2 + ln l, evaluated in double and rounded once to fp32, so the
-// LSE a tile hands to the merge carries only its own fp32 rounding.
+// sum l > 0: (m + e) ln 2 + ln f with l = f 2^e, f in [0.5, 1).  m + e is an
+// exact small integer, its product with the high part of ln 2 (a Cody-Waite
+// split) is exact, and the small terms go into the last addition, so the
+// result carries about one fp32 rounding, as a double evaluation rounded to
+// fp32 would -- without FP64 arithmetic, which is slow on this part (a double
+// log per row had cost microseconds of every launch's tail).
 __device__ __forceinline__ float lse_of(float m, float l) {
-  return static_cast<float>(static_cast<double>(m) * kLn2 + log(static_cast<double>(l)));
+  if (m == -INFINITY || !(l > 0.f)) return m * kLn2Hi + logf(l);   // -inf / degenerate
+  int e;
+  const float f = frexpf(l, &e);
+  const float t = m + static_cast<float>(e);
+  return t * kLn2Hi + fmaf(t, kLn2Lo, logf(f));
 }
 
 __device__ __forceinline__ float ref_ceil(float x) {

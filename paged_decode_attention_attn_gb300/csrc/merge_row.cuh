@@ -92,8 +92,9 @@ __device__ __forceinline__ void merge_row(const float* out_parts, const float* l
     }
     wsum = ws;
   }
-  if (lane == 0)
-    *lse_out = static_cast<float>(static_cast<double>(big_m) + log(static_cast<double>(wsum)));
+  // wsum is in [1, n] (the largest partial weighs 1): one fp32 rounding of
+  // big_m + ln(wsum); a single partial gives big_m exactly.
+  if (lane == 0) *lse_out = big_m + logf(wsum);
 }
 
 }  // namespace mergerow
