@@ -158,3 +158,37 @@ def test_tile_staged_route_is_bit_identical_to_resident_tile_launches(D, make):
     host.close()
     del staged, host, t, res
     _free()
+
+
+def test_bench_launch_configuration_matches_oracle(D):
+    """The bench's configuration (fused launches with early page loads,
+    replayed as a CUDA graph) returns the eager route's bits at full size,
+    and sampled (layer, request) pairs match the oracle."""
+    w = wl.four_requests_31744(n_layers=4)
+    t = wl.materialize(w, "cuda")
+    eager = D.ResidentDecode(w, {k: v.clone() for k, v in t.items()})
+    torch.cuda.synchronize()
+    eager.step()
+    torch.cuda.synchronize()
+    dec = D.ResidentDecode(w, t, kv_ready=True)
+    torch.cuda.synchronize()
+    dec.step()                                   # warm-up (also stores the new rows)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    dec.stream = cap
+    with torch.cuda.graph(graph, stream=cap):
+        dec.step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    assert dec.kernel_status() == 0
+    assert torch.equal(dec.o.out, eager.o.out) and torch.equal(dec.o.lse, eager.o.lse)
+    for i, r in [(0, 0), (3, 2)]:
+        ref = oracle_request(w, t, i, r, gather_on_device=True)
+        o = dec.o
+        assert_close_to_oracle(o.tile_out[i, r], o.tile_lse[i, r], o.out[i, r], o.lse[i, r], ref,
+                               w.tiles[r], f"graph layer {i} request {r}")
+    del dec, eager, graph, t
+    _free()
