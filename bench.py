@@ -16,6 +16,8 @@ LSE merge.
          launch time (CUDA events on the launching stream), against the
          measured HBM copy bandwidth.
   cpu_baseline  the fp64 NumPy oracle on a bounded sample on the host cores.
+  merge_stress  the standalone FP32 LSE merge on 64 requests x 24 heads x 256
+         with 1..64 partials each: GB/s of partials read and rows written.
 
 python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -40,7 +42,10 @@ UNIT = "GB/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_kernel_4x31744.md")
-KERNEL_SOURCE = os.path.join(ROOT, "paged_decode_attention_attn_gb300", "csrc", "decode_attn.cu")
+# the decode kernel's translation unit: the .cu file and the headers it includes
+KERNEL_SOURCES = [os.path.join(ROOT, "paged_decode_attention_attn_gb300", "csrc", f)
+                  for f in ("decode_attn.cu", "merge_row.cuh", "ptx.cuh", "common.h")] + [
+                      os.path.join(ROOT, "include", "pagedattn.h")]
 
 
 def parse_args(argv=None):
@@ -66,6 +71,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-compact", action="store_true",
                     help="skip the end-to-end run with published pages staged compact")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-merge-arm", action="store_true",
+                    help="skip the standalone LSE-merge measurement on the merge-stress shape")
     ap.add_argument("--cpu-workers", type=int, default=0)
     ap.add_argument("--bus-model", action="store_true",
                     help="fit the staged route's latency model over 32K-262K tokens "
@@ -179,9 +186,13 @@ def hbm_peak():
 
 def recorded_traffic():
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel source as it is now (else None)."""
+    the kernel's sources as they are now (sha256 over the files of
+    KERNEL_SOURCES in order), else None."""
     try:
-        src = hashlib.sha256(open(KERNEL_SOURCE, "rb").read()).hexdigest()
+        h = hashlib.sha256()
+        for f in KERNEL_SOURCES:
+            h.update(open(f, "rb").read())
+        src = h.hexdigest()
         fields = {}
         for line in open(TRAFFIC_FILE):
             if ":" in line and line.strip().startswith("- "):
@@ -413,6 +424,7 @@ def run_ours(args):
         kern_how = "events around each launch of an eager run of the same steps"
     achieved = kv_bytes_layer / (kern_ms / 1e3) / 1e9
     null_ms = null_arm(args, w, t, D, B, dev, fused, kv_ready)
+    merge_stress = None if args.no_merge_arm else merge_arm(dev, B)
 
     # ---- staged route, end to end through host buffers ----
     e2e = e2e_compact = e2e_tiled = None
@@ -479,6 +491,8 @@ def run_ours(args):
             "step_launch": f"CUDA graph of the {launches_per_step} launches of one step, "
                            "replayed per step",
         }
+        if merge_stress is not None:
+            line["merge_stress"] = merge_stress
         if e2e is not None:
             line["e2e"] = e2e
         if e2e_compact is not None:
@@ -543,6 +557,47 @@ def null_arm(args, w, t, D, B, dev, fused, kv_ready):
     if nd.kernel_status() != 0:
         raise RuntimeError("null arm kernel status non-zero")
     return e0.elapsed_time(e1) / n
+
+
+def merge_arm(dev, B, iters=50):
+    """The standalone FP32 LSE merge on the merge-stress shape: 64 requests x
+    24 heads x 256, 1..64 partials per request, partial LSEs spread +-80.  The
+    partials (~51 MB) fit in L2, so a 256 MiB buffer is written before every
+    launch; each launch is timed alone with CUDA events on its stream."""
+    import torch
+    from paged_decode_attention_attn_gb300 import workloads as wl
+    H, Dh = 24, 256
+    offsets = wl.merge_stress_layout()
+    out_parts, lse_parts = wl.merge_stress_partials_device(offsets, H, Dh, dev)
+    n_req = len(offsets) - 1
+    off_d = torch.as_tensor(offsets, dtype=torch.int32).to(dev)
+    out = torch.empty((n_req, H, Dh), dtype=torch.float32, device=dev)
+    lse = torch.empty((n_req, H), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(iters)]
+    for _ in range(3):
+        B.lse_merge(out_parts, lse_parts, off_d, out, lse, stream=stream)
+    torch.cuda.synchronize(dev)
+    for e0, e1 in ev:
+        flush.fill_(1)
+        e0.record(stream)
+        B.lse_merge(out_parts, lse_parts, off_d, out, lse, stream=stream)
+        e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
+    n_parts = int(offsets[-1])
+    # partials read once (outputs and LSEs), offsets read, merged rows written
+    nbytes = (n_parts * H * (Dh + 1) + n_req * H * (Dh + 1)) * 4 + (n_req + 1) * 4
+    gbs = nbytes / (ms / 1e3) / 1e9
+    peak, peak_kind = hbm_peak()
+    return {"value": round(gbs, 1), "unit": "GB/s", "kernel": "lse_merge_kernel",
+            "median_launch_us": round(ms * 1e3, 2), "launches": iters,
+            "bytes_per_launch": nbytes, "partials": n_parts, "requests": n_req,
+            "frac_of_hbm_peak": round(gbs / peak, 4), "peak_kind": peak_kind,
+            "l2": "256 MiB buffer written before every launch (partials fit in L2)",
+            "workload": "64 requests x 24 heads x 256, 1..64 partials each, LSE +-80"}
 
 
 def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):

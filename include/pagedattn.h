@@ -258,7 +258,7 @@ int paged_decode_attn_test_stall(int iteration, uint64_t wait_limit_ns);
  *   out_parts    device fp32 [n_parts][H][D];  lse_parts device fp32 [n_parts][H]
  *   part_offsets device int32 [B+1], non-decreasing, part_offsets[0] = 0.
  *   out, lse     device fp32 [B][H][D], [B][H].
- * D must be a multiple of 4 and the fp32 arrays 16-byte aligned. */
+ * D must be a positive multiple of 4 and the fp32 arrays 16-byte aligned. */
 int lse_merge(const float* out_parts, const float* lse_parts,
               const int32_t* part_offsets, int B, int H, int D,
               float* out, float* lse, cudaStream_t stream);

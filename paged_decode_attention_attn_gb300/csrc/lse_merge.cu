@@ -3,11 +3,13 @@
 // Merge rule ("KV-cache engineering", section "Exact recent pages, compact
 // older pages"): weight each partial by exp(LSE_i - max LSE), sum the weighted
 // outputs, divide by the summed weights, and return max + log(sum) as the
-// merged LSE.  One warp per (request, head); partials are read in increasing
-// order so the result is deterministic, and the division by the summed
-// weights (not a multiply by its reciprocal) returns a single partial bit for
-// bit.  The merge reads ~H*D*4 bytes per partial once; it is tiny next to the
-// attention and is bound by L2/HBM latency, not bandwidth.
+// merged LSE.  Each output column sums its partials in increasing order so
+// the result is deterministic (and equal to the decode kernel's fused merge),
+// and the division by the summed weights (not a multiply by its reciprocal)
+// returns a single partial bit for bit.  The merge reads H*(D+1)*4 bytes per
+// partial once; with up to 64 partials per request the time is set by the
+// longest rows, so each row is spread over several warps and each warp keeps
+// several partials' loads in flight.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -20,22 +22,32 @@ namespace pa {
 namespace merge {
 
 constexpr int kWarpsPerBlock = 8;
+constexpr int kLoadBatch = 8;  // partials loaded ahead of their arithmetic per warp
+constexpr int kVec = 1;        // float4 columns per lane: a warp takes 128 columns of a row
+constexpr int kChunkCols = 32 * kVec;
 
+// One warp per (request, head, 128-column chunk): a row with many partials is
+// read by D/128 warps at once.  The chunk-0 warp writes the row's LSE.
 __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     lse_merge_kernel(const float* __restrict__ out_parts, const float* __restrict__ lse_parts,
-                     const int32_t* __restrict__ offsets, int B, int H, int D,
+                     const int32_t* __restrict__ offsets, int B, int H, int D, int n_chunks,
                      float* __restrict__ out, float* __restrict__ lse) {
   ptx::launch_dependents();
   ptx::grid_dependency_wait();  // the partials come from the previous kernel
   const int lane = threadIdx.x & 31;
   const long long wid = (long long)blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (wid >= (long long)B * H) return;
-  const int b = static_cast<int>(wid / H);
-  const int h = static_cast<int>(wid - (long long)b * H);
+  if (wid >= (long long)B * H * n_chunks) return;
+  const long long row = wid / n_chunks;
+  const int chunk = static_cast<int>(wid - row * n_chunks);
+  const int b = static_cast<int>(row / H);
+  const int h = static_cast<int>(row - (long long)b * H);
   const int p0 = offsets[b];
   const int n = offsets[b + 1] - p0;
-  mergerow::merge_row<false>(out_parts, lse_parts, p0, n, H, h, D,
-                             out + ((size_t)b * H + h) * D, lse + (size_t)b * H + h, lane);
+  const int c_lo = chunk * kChunkCols;
+  const int c_hi = min(D / 4, c_lo + kChunkCols);
+  mergerow::merge_cols<false, kLoadBatch, kVec>(out_parts, lse_parts, p0, n, H, h, D, c_lo, c_hi,
+                                                out + (size_t)row * D,
+                                                chunk == 0 ? lse + row : nullptr, lane);
 }
 
 // One warp per row: copy rows[b] into the pool row of token positions[b].
@@ -77,16 +89,17 @@ extern "C" int lse_merge(const float* out_parts, const float* lse_parts,
   PA_REQUIRE(B >= 0 && H >= 0 && D >= 0, "negative size");
   if ((long long)B * H == 0) return PA_OK;
   PA_REQUIRE(part_offsets && out && lse, "null pointer argument");
-  PA_REQUIRE(D % 4 == 0, "D (%d) must be a multiple of 4", D);
+  PA_REQUIRE(D > 0 && D % 4 == 0, "D (%d) must be a positive multiple of 4", D);
   PA_REQUIRE(reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
                  reinterpret_cast<uintptr_t>(out_parts) % 16 == 0,
              "out and out_parts must be 16-byte aligned");
-  const long long warps = (long long)B * H;
+  const int n_chunks = (D / 4 + pa::merge::kChunkCols - 1) / pa::merge::kChunkCols;
+  const long long warps = (long long)B * H * n_chunks;
   const long long blocks = (warps + pa::merge::kWarpsPerBlock - 1) / pa::merge::kWarpsPerBlock;
   PA_REQUIRE(blocks < (1ll << 31), "too many (request, head) pairs");
   PA_CHECK_CUDA(pa::launch_dependent(pa::merge::lse_merge_kernel, dim3((unsigned)blocks),
                                      dim3(pa::merge::kWarpsPerBlock * 32), 0, stream, out_parts,
-                                     lse_parts, part_offsets, B, H, D, out, lse));
+                                     lse_parts, part_offsets, B, H, D, n_chunks, out, lse));
   PA_CHECK_CUDA(cudaGetLastError());
   return PA_OK;
 }

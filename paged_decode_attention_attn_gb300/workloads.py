@@ -314,3 +314,27 @@ def merge_stress(seed: int = 5, n_requests: int = 64, n_heads: int = 24,
         values.append(vr)
         bias.append(br)
     return MergeStressCase(logits, values, bias, n_heads, head_dim)
+
+
+def merge_stress_layout(seed: int = 5, n_requests: int = 64, max_parts: int = 64) -> np.ndarray:
+    """Partial offsets int32 [B+1] of a merge-stress-shaped input: request r
+    owns partials [off[r], off[r+1]), a count uniform in 1..max_parts.  Used to
+    time the merge on synthetic partials (the values then come from
+    ``merge_stress_partials_device``)."""
+    rng = np.random.default_rng([seed, 77])
+    counts = rng.integers(1, max_parts, size=n_requests, endpoint=True)
+    return np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+
+
+def merge_stress_partials_device(offsets: np.ndarray, n_heads: int, head_dim: int, device,
+                                 seed: int = 5, spread: float = 80.0):
+    """Random fp32 partial outputs N(0,1) [P][H][D] and partial LSEs uniform in
+    [-spread, spread] [P][H] on the device, for timing the merge."""
+    n_parts = int(offsets[-1])
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 7919 + 3)
+    out_parts = torch.randn((n_parts, n_heads, head_dim), generator=g, device=device,
+                            dtype=torch.float32)
+    lse_parts = (torch.rand((n_parts, n_heads), generator=g, device=device,
+                            dtype=torch.float32) * 2 - 1) * spread
+    return out_parts, lse_parts

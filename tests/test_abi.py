@@ -86,6 +86,7 @@ def test_merge_and_append_argument_checks(B):
     fake = 1 << 20
     assert B.lib.lse_merge(fake, fake, fake, 2, 24, 254, fake, fake, None) == B.PA_ERR_INVALID
     assert B.lib.lse_merge(fake, fake, fake, 0, 24, 256, fake, fake, None) == B.PA_OK
+    assert B.lib.lse_merge(fake, fake, fake, 2, 24, 0, fake, fake, None) == B.PA_ERR_INVALID
     assert B.lib.kv_append_rows(fake, 4, fake, 4, fake, fake, 1, 4008, None, None) == \
         B.PA_ERR_INVALID
     assert B.lib.kv_append_rows(fake, 4, fake, 4, fake, fake + 8, 1, 4096, None, None) == \

@@ -217,6 +217,32 @@ def test_lse_merge_stress_matches_unsplit_softmax(B):
         assert max_abs(lse[r].double().cpu(), ml) <= 1e-4
 
 
+@pytest.mark.parametrize("D", [4, 12, 128, 132, 256, 260, 520])
+def test_lse_merge_head_dims_and_partial_counts(B, D):
+    """Rows of any width (one or several 128-column warps, a ragged last one)
+    and partial counts on both sides of the load batch, against the oracle's
+    fp64 merge of the same fp32 partials."""
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(D)
+    H = 3
+    counts = [1, 2, 7, 8, 9, 15, 16, 17, 33, 64]
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    P = int(offsets[-1])
+    parts = torch.randn((P, H, D), generator=g, device=dev)
+    lses = (torch.rand((P, H), generator=g, device=dev) * 2 - 1) * 80
+    out = torch.full((len(counts), H, D), 7.0, device=dev)
+    lse = torch.full((len(counts), H), 7.0, device=dev)
+    B.lse_merge(parts, lses, torch.as_tensor(offsets, device=dev), out, lse)
+    torch.cuda.synchronize()
+    o64 = parts.double().cpu().numpy()
+    l64 = lses.double().cpu().numpy()
+    for r in range(len(counts)):
+        mo, ml = oracle.lse_merge(o64[offsets[r]:offsets[r + 1]], l64[offsets[r]:offsets[r + 1]])
+        assert max_abs(out[r].double().cpu(), mo) <= 1e-5, (D, counts[r])
+        assert max_abs(lse[r].double().cpu(), ml) <= 1e-4, (D, counts[r])
+    assert torch.equal(out[0], parts[0]) and torch.equal(lse[0], lses[0])
+
+
 def test_lse_merge_identity_and_edges(B):
     dev = "cuda"
     g = torch.Generator(device=dev).manual_seed(1)
