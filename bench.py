@@ -12,6 +12,8 @@ LSE merge.
          Q and the new rows go host->device, every layer's history is staged
          from pinned host memory into a 2-slot device arena, the tail rows are
          written back, and the outputs come back to the host.
+  e2e_resident  the resident route through the same calls with host buffers:
+         history in HBM, per step Q and new rows in, merged outputs out.
   roofline  the attention kernel alone: algorithmic bytes per launch / mean
          launch time (CUDA events on the launching stream), against the
          measured HBM copy bandwidth.
@@ -425,6 +427,15 @@ def run_ours(args):
     achieved = kv_bytes_layer / (kern_ms / 1e3) / 1e9
     null_ms = null_arm(args, w, t, D, B, dev, fused, kv_ready)
     merge_stress = None if args.no_merge_arm else merge_arm(dev, B)
+    e2e_resident = None
+    if not args.no_e2e:
+        e2e_resident = run_e2e_resident(args, w, t, res.o, graph, dev)
+        secs = max_over_ranks(e2e_resident.pop("_secs"), world)
+        e2e_resident["value"] = round(whole_job_gbs(kv_bytes, e2e_resident["steps"], secs * 1e3,
+                                                    world), 2)
+        e2e_resident["ms_per_step"] = round(1e3 * secs / e2e_resident["steps"], 4)
+        if res.kernel_status() != 0:
+            raise RuntimeError("kernel status non-zero after the resident e2e steps")
 
     # ---- staged route, end to end through host buffers ----
     e2e = e2e_compact = e2e_tiled = None
@@ -495,6 +506,8 @@ def run_ours(args):
             line["merge_stress"] = merge_stress
         if e2e is not None:
             line["e2e"] = e2e
+        if e2e_resident is not None:
+            line["e2e_resident"] = e2e_resident
         if e2e_compact is not None:
             line["e2e_compact"] = e2e_compact
         if e2e_tiled is not None:
@@ -598,6 +611,40 @@ def merge_arm(dev, B, iters=50):
             "frac_of_hbm_peak": round(gbs / peak, 4), "peak_kind": peak_kind,
             "l2": "256 MiB buffer written before every launch (partials fit in L2)",
             "workload": "64 requests x 24 heads x 256, 1..64 partials each, LSE +-80"}
+
+
+def run_e2e_resident(args, w, t, o, graph, dev):
+    """The resident route with host buffers: the history stays in HBM (the
+    state a serving process keeps); per step the queries and new rows are
+    copied in from pinned host memory, the step's graph runs, and the merged
+    outputs and LSEs are copied back.  Host wall time over the steps."""
+    import torch
+    q_host = t["q"].cpu().pin_memory()
+    rows_host = t["new_rows"].cpu().pin_memory()
+    res_out, res_lse = (o.tile_out, o.tile_lse) if w.n_tiles == 1 else (o.out, o.lse)
+    out_host = torch.empty(res_out.shape, dtype=torch.float32).pin_memory()
+    lse_host = torch.empty(res_lse.shape, dtype=torch.float32).pin_memory()
+
+    def step():
+        t["q"].copy_(q_host, non_blocking=True)
+        t["new_rows"].copy_(rows_host, non_blocking=True)
+        graph.replay()
+        out_host.copy_(res_out, non_blocking=True)
+        lse_host.copy_(res_lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    secs = time.perf_counter() - t0
+    return {"unit": UNIT, "_secs": secs, "steps": args.steps,
+            "h2d_bytes_per_step": (q_host.numel() + rows_host.numel()) * 2,
+            "d2h_bytes_per_step": (out_host.numel() + lse_host.numel()) * 4,
+            "route": "history resident in HBM; per step queries and new rows in from pinned "
+                     "host memory, the step's graph, merged outputs and LSEs out"}
 
 
 def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
