@@ -69,3 +69,34 @@ def test_random_cases(D, seed):
         ref = oracle_request(w, t, 0, r)
         assert_close_to_oracle(o.tile_out[0, r], o.tile_lse[0, r], o.out[0, r], o.lse[0, r], ref,
                                w.tiles[r], f"seed {seed} request {r}")
+
+
+def test_sixty_four_tiles_per_request(D):
+    """64 tiles per request (the merge-stress partial count): uneven, empty
+    and single-token tiles cut from histories of 1 to 9,000 tokens."""
+    rng = np.random.default_rng(64)
+    lengths = [9000, 1, 4097]
+    tiles = []
+    for L in lengths:
+        cuts = np.sort(rng.integers(0, L + 1, size=63))
+        edges = np.concatenate([[0], cuts, [L]])
+        tiles.append([(int(a), int(b)) for a, b in zip(edges[:-1], edges[1:])])
+    w = wl.custom(lengths, tiles, seed=640, n_spare=3, n_layers=1)
+    assert w.n_tiles == 64
+    t = wl.materialize(w, "cuda")
+    runs = {}
+    for name, kw in (("fused", dict(fused=True)), ("three", dict(fused=False))):
+        tc = {k: v.clone() for k, v in t.items()}
+        dec = D.ResidentDecode(w, tc, **kw)
+        torch.cuda.synchronize()
+        dec.step()
+        torch.cuda.synchronize()
+        assert dec.kernel_status() == 0, name
+        runs[name] = dec
+    a, b = runs["fused"].o, runs["three"].o
+    assert torch.equal(a.out, b.out) and torch.equal(a.lse, b.lse)
+    assert torch.equal(a.tile_out, b.tile_out) and torch.equal(a.tile_lse, b.tile_lse)
+    for r in range(w.batch):
+        ref = oracle_request(w, t, 0, r)
+        assert_close_to_oracle(a.tile_out[0, r], a.tile_lse[0, r], a.out[0, r], a.lse[0, r], ref,
+                               w.tiles[r], f"request {r}")
