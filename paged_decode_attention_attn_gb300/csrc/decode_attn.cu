@@ -272,13 +272,11 @@ __device__ __forceinline__ void finish_unit(const Params<kMaxUnits>& p, const Sh
   if (p.m_out == nullptr) return;
   ptx::named_barrier(1, kConsumers);       // the unit's outputs are all stored
   if (ct == 0) {
-    __threadfence();
-    const int prev = atomicAdd(p.req_counters + b * p.Hkv + g, 1);
+    const int prev = ptx::atomic_add_acq_rel_gpu(p.req_counters + b * p.Hkv + g, 1);
     *sh.fin_flag = (prev == p.T - 1) ? 1 : 0;
   }
   ptx::named_barrier(1, kConsumers);
   if (*sh.fin_flag) {
-    __threadfence();
     for (int r = warp; r < p.G; r += kConsumerWarps) {
       const int h = g * p.G + r;
       mergerow::merge_row<true>(p.out, p.lse, b * p.T, p.T, p.Hq, h, kD,
@@ -842,12 +840,13 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     }
     if (!single) {
       // The last CTA to finish this unit merges every partial, in CTA order.
-      // The barrier orders every thread's partial before thread 0's fence,
-      // which publishes them all at device scope before the count.
+      // The barrier orders every thread's partial before thread 0's
+      // acquire-release count, which publishes them at device scope and, in
+      // the last CTA, makes every other CTA's partial visible; the barrier
+      // after it extends that to the CTA's threads.
       ptx::named_barrier(1, kConsumers);
       if (ct == 0) {
-        __threadfence();
-        const int prev = atomicAdd(p.counters + u, 1);
+        const int prev = ptx::atomic_add_acq_rel_gpu(p.counters + u, 1);
         *sh.merge_flag = (prev == U.n_parts - 1) ? 1 : 0;
       }
       ptx::named_barrier(1, kConsumers);
@@ -855,7 +854,6 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         // One CTA finishes the unit while the rest of the grid is idle, so
         // this is latency-bound: every thread issues all of its loads before
         // it does any arithmetic (one L2 round trip per phase).
-        __threadfence();
         const int n = U.n_parts;
         float* wts = sh.xo;                 // [part][kMaxG]
         float* row_l = sh.xml;              // [kMaxG]
