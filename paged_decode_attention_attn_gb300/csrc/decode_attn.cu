@@ -806,9 +806,13 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     const bool single = U.n_parts == 1;
     int slot = 0;
     if (!single) slot = U.part_base + (int)blockIdx.x - cta_of(pf, p.total_pages, p.grid);
-    for (int idx = ct; idx < G * kD; idx += kConsumers) {
-      const int row = idx / kD;
-      const int d = idx - row * kD;
+    // Four consecutive output dims per thread and step (float4 exchange
+    // reads and stores): the combine sits on the critical path of the CTA
+    // that finishes last.
+    constexpr int kDimVec = kD / 4;
+    for (int idx = ct; idx < G * kDimVec; idx += kConsumers) {
+      const int row = idx / kDimVec;
+      const int dv = idx - row * kDimVec;
       float mw[kGroups];
       float big_m = -INFINITY;
       bool nan = false;
@@ -818,21 +822,29 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         nan |= (mw[w2] != mw[w2]);
         big_m = fmaxf(big_m, mw[w2]);
       }
-      float o = 0.f, l = 0.f;
+      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+      float l = 0.f;
 #pragma unroll
       for (int w2 = 0; w2 < kGroups; ++w2) {
         const float a = ref_weight(mw[w2], big_m);
-        o = fmaf(a, sh.xo[(w2 * kMaxG + row) * kXRow + d], o);
+        const float4 x =
+            *reinterpret_cast<const float4*>(sh.xo + (w2 * kMaxG + row) * kXRow + 4 * dv);
+        o.x = fmaf(a, x.x, o.x);
+        o.y = fmaf(a, x.y, o.y);
+        o.z = fmaf(a, x.z, o.z);
+        o.w = fmaf(a, x.w, o.w);
         l = fmaf(a, sh.xml[(w2 * kMaxG + row) * 2 + 1], l);
       }
       if (nan) big_m = __int_as_float(0x7fc00000);
       if (single) {
         const size_t orow = (size_t)bt * p.Hq + g * G + row;
-        p.out[orow * kD + d] = nan ? big_m : o / l;
-        if (d == 0) p.lse[orow] = nan ? big_m : lse_of(big_m, l);
+        reinterpret_cast<float4*>(p.out + orow * kD)[dv] =
+            nan ? make_float4(big_m, big_m, big_m, big_m)
+                : make_float4(o.x / l, o.y / l, o.z / l, o.w / l);
+        if (dv == 0) p.lse[orow] = nan ? big_m : lse_of(big_m, l);
       } else {
-        p.part_o[((size_t)slot * kMaxG + row) * kD + d] = o;
-        if (d == 0) {
+        reinterpret_cast<float4*>(p.part_o + ((size_t)slot * kMaxG + row) * kD)[dv] = o;
+        if (dv == 0) {
           p.part_ml[((size_t)slot * kMaxG + row) * 2 + 0] = big_m;
           p.part_ml[((size_t)slot * kMaxG + row) * 2 + 1] = l;
         }
