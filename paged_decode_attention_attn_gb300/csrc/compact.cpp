@@ -159,7 +159,7 @@ struct kv_compactor {
       {
         std::lock_guard<std::mutex> lk(mu);
         --active;
-        if (active == 0 && jobs.empty()) cv_idle.notify_all();
+        if (active == 0 && (jobs.empty() || hold)) cv_idle.notify_all();
       }
     }
   }
@@ -300,6 +300,7 @@ extern "C" int kv_compactor_hold(kv_compactor* c, int hold) {
     c->hold = hold != 0;
   }
   c->cv_work.notify_all();
+  c->cv_idle.notify_all();   // a waiter for idleness re-checks: held counts as idle
   return PA_OK;
 }
 

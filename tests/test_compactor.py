@@ -196,3 +196,26 @@ def test_thread_count_does_not_change_the_bytes(B):
         outs.append([h.store[l][r].numpy().tobytes() for l in range(2) for r in range(2)])
         c.close()
     assert outs[0] == outs[1]
+
+
+def test_hold_during_conversion_ends_an_idle_wait_promptly(B):
+    # one converter thread, many queued pages: holding it while a page is in
+    # progress leaves the rest queued, and a waiter for idleness returns as
+    # soon as that page is done (held counts as idle) instead of at its timeout
+    import time
+    h = History(B, [64 * 40], n_layers=32)     # ~tens of ms per page (32 layers each)
+    c = h.make(threads=1)
+    c.mark_written(0, 40)
+    time.sleep(0.005)                            # the thread is inside its first page
+    c.hold(True)
+    t0 = time.perf_counter()
+    with pytest.raises(B.PagedAttnError) as e:
+        c.wait_idle(20000)
+    assert e.value.code == B.PA_ERR_ORDER
+    assert time.perf_counter() - t0 < 5.0
+    st = c.states(0)
+    assert B.PA_PAGE_QUEUED in st                       # the hold stopped the queue
+    c.hold(False)
+    c.wait_idle()
+    assert c.states(0) == [B.PA_PAGE_PUBLISHED] * 40
+    c.close()
