@@ -48,6 +48,11 @@
  *     message is available from kv_last_error().  No C++ exception crosses
  *     the ABI.
  *   - Layouts are dense row-major in the order the brackets list.
+ *   - Threads: the decode, merge and row-append entry points keep no state
+ *     between calls (except the fixed scratch of the _noalloc variant) and
+ *     may be called from several host threads.  An arena, planner or
+ *     compactor handle is used by one thread at a time (the caller
+ *     serialises); distinct handles are independent.
  *
  * Data layout (the "pool"): a page is PA_PAGE_TOKENS consecutive token rows;
  * a row is [K of kv heads 0..Hkv-1 | V of kv heads 0..Hkv-1], head_dim bf16
