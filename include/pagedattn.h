@@ -321,7 +321,8 @@ typedef struct {
 /* A run of consecutive logical pages of one request.  host_rows != NULL: a
  * staged run, n_rows rows (<= n_pages * page_tokens) are copied from pinned
  * host memory into the slot.  host_rows == NULL: a resident run whose pages
- * already sit in the arena at resident_page, resident_page + 1, ... */
+ * already sit in the arena at resident_page, resident_page + 1, ... (outside
+ * the staging slots; a run overlapping them is refused). */
 typedef struct {
     int32_t     logical_page;
     int32_t     n_pages;

@@ -383,6 +383,12 @@ int validate_stage(kv_arena* a, const kv_stage_req* reqs, int n_reqs) {
       } else {
         PA_REQUIRE(run.resident_page >= 0 && run.resident_page + run.n_pages <= a->arena_pages,
                    "request %d run %d: resident pages outside the arena", r.request, k);
+        const int64_t slots_end = d.slot_first_page + (int64_t)d.n_slots * d.slot_pages;
+        PA_REQUIRE(run.resident_page + run.n_pages <= d.slot_first_page ||
+                       run.resident_page >= slots_end,
+                   "request %d run %d: resident pages [%" PRId64 ", +%d) overlap the staging "
+                   "slots [%" PRId64 ", %" PRId64 ")",
+                   r.request, k, run.resident_page, run.n_pages, d.slot_first_page, slots_end);
       }
     }
   }

@@ -201,6 +201,8 @@ def test_validation(B):
         [(4, 1, [staged(0, 1, 0x1000)])],                       # request >= max_requests
         [(0, 1, [staged(0, 1, 0x1000)]), (0, 2, [staged(1, 1, 0x2000)])],  # request twice
         [(0, 1, [resident(0, 2, 19)])],                         # resident past the arena
+        [(0, 1, [resident(0, 2, 3)])],                          # resident into slot 0
+        [(0, 1, [resident(0, 1, 12)])],                         # resident inside slot 1
     ]
     for reqs in bad:
         with pytest.raises(B.PagedAttnError) as e:
