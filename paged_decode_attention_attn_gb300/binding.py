@@ -517,26 +517,12 @@ class Arena:
         logical_page, n_pages and either host_rows (address) + n_rows,
         host_compact (address of compact pages) + n_rows = n_pages * 64, or
         resident_page.  Returns (slot, page_table_address)."""
-        reqs = (KvStageReq * len(requests))()
-        keep = []
-        for i, (request, owner, runs) in enumerate(requests):
-            arr = (KvPageRun * max(1, len(runs)))()
-            for k, r in enumerate(runs):
-                arr[k].logical_page = r["logical_page"]
-                arr[k].n_pages = r["n_pages"]
-                arr[k].n_rows = r.get("n_rows", 0)
-                arr[k].host_rows = r.get("host_rows")
-                arr[k].resident_page = r.get("resident_page", 0)
-                arr[k].host_compact = r.get("host_compact")
-            keep.append(arr)
-            reqs[i].request = request
-            reqs[i].n_runs = len(runs)
-            reqs[i].runs = ctypes.cast(arr, ctypes.POINTER(KvPageRun))
-            reqs[i].owner = owner
+        reqs, keep = self._stage_reqs(requests)
         slot = ctypes.c_int(-1)
         table = ctypes.c_void_p()
         _check(lib.kv_stage_layer(self.handle, layer, reqs, len(requests), ctypes.byref(slot),
                                   ctypes.byref(table)))
+        del keep
         return slot.value, table.value
 
     def mark_attention_done(self, layer: int):
@@ -544,13 +530,7 @@ class Arena:
 
     def writeback_tail(self, layer: int, tails):
         """tails: list of (request, position, host_row_address, owner)."""
-        arr = (KvTailReq * max(1, len(tails)))()
-        for i, (request, position, host_row, owner) in enumerate(tails):
-            arr[i].request = request
-            arr[i].position = position
-            arr[i].host_row = host_row
-            arr[i].owner = owner
-        _check(lib.kv_writeback_tail(self.handle, layer, arr, len(tails)))
+        _check(lib.kv_writeback_tail(self.handle, layer, self._tail_reqs(tails), len(tails)))
 
     @staticmethod
     def _stage_reqs(requests):
