@@ -192,3 +192,35 @@ def test_bench_launch_configuration_matches_oracle(D):
                                w.tiles[r], f"graph layer {i} request {r}")
     del dec, eager, graph, t
     _free()
+
+
+@pytest.mark.parametrize("n_slots", [1, 2])
+def test_staged_route_over_many_steps(D, n_slots):
+    """Eight consecutive steps of the staged route, with no host wait between
+    them (slots refilled while earlier layers' attention and write-back may
+    still run): every step's outputs equal the resident route's bit for bit."""
+    make, _ = FULL["4x31744"]
+    w = make(n_layers=3)
+    t = wl.materialize(w, "cuda")
+    host = D.HostHistory(w, t)
+    staged = D.StagedDecode(w, t, host, n_slots=n_slots)
+    res = D.ResidentDecode(w, t)
+    res.step()
+    torch.cuda.synchronize()
+    outs = []
+    for _ in range(8):
+        staged.step()
+        outs.append(tuple(x.clone() for x in (staged.o.tile_out, staged.o.tile_lse,
+                                              staged.o.out, staged.o.lse)))
+    staged.drain()
+    torch.cuda.synchronize()
+    assert res.kernel_status() == 0 and staged.kernel_status() == 0
+    ref = (res.o.tile_out, res.o.tile_lse, res.o.out, res.o.lse)
+    for k, o in enumerate(outs):
+        assert all(torch.equal(a, b) for a, b in zip(o, ref)), f"step {k}"
+    st = staged.handle.stats()
+    assert st.stage_generation == 8 * w.n_layers and st.quarantined == 0
+    staged.close()
+    host.close()
+    del staged, res, host, t
+    _free()
