@@ -100,3 +100,24 @@ def test_sixty_four_tiles_per_request(D):
         ref = oracle_request(w, t, 0, r)
         assert_close_to_oracle(a.tile_out[0, r], a.tile_lse[0, r], a.out[0, r], a.lse[0, r], ref,
                                w.tiles[r], f"request {r}")
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.3, 0.01, 0.125])
+@pytest.mark.parametrize("cuda_core", [False, True], ids=["tensor", "cuda-core"])
+def test_softmax_scale_is_applied(D, scale, cuda_core):
+    """Scales other than 1/16 (peakier and flatter softmaxes) match the oracle
+    on both kernel variants."""
+    geo = wl.Geometry(scale=scale)
+    w = wl.custom([700, 2049], [[(0, 300), (300, 700)], [(0, 2049)]], seed=31, n_spare=2,
+                  geometry=geo)
+    t = wl.materialize(w, "cuda")
+    dec = D.ResidentDecode(w, t, cuda_core=cuda_core, fused=not cuda_core)
+    torch.cuda.synchronize()
+    dec.step()
+    torch.cuda.synchronize()
+    assert dec.kernel_status() == 0
+    o = dec.o
+    for r in range(w.batch):
+        ref = oracle_request(w, t, 0, r)
+        assert_close_to_oracle(o.tile_out[0, r], o.tile_lse[0, r], o.out[0, r], o.lse[0, r], ref,
+                               w.tiles[r], f"scale {scale} request {r}")
