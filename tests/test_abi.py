@@ -76,6 +76,10 @@ def test_decode_argument_checks(B):
     assert _call_decode(B, ok_tiles, ws_bytes=1024) == B.PA_ERR_INVALID  # workspace too small
     assert _call_decode(B, ok_tiles, ws_ptr=(1 << 20) + 16) == B.PA_ERR_INVALID  # misaligned
     assert "workspace" in B.last_error()
+    # 2^25 pages = 2^31 rows: past the 32-bit row coordinates of the page loads
+    assert _call_decode(B, ok_tiles, pool_pages=(1 << 25)) == B.PA_ERR_INVALID
+    assert "pool too large" in B.last_error()
+    assert _call_decode(B, ok_tiles, pool_pages=0) == B.PA_ERR_INVALID
     # zero requests is a no-op
     arr = np.zeros((0, 1, 2), dtype=np.int32)
     assert B.lib.paged_decode_attn_lse(0, 0, 0, 0, 0, arr.ctypes.data, 0, 1, 24, 4, 256, 1.0, 0,
