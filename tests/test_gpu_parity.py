@@ -113,6 +113,43 @@ def test_physical_placement_does_not_change_bits(B, D, cuda_core):
     assert torch.equal(a.o.out, b.o.out) and torch.equal(a.o.lse, b.o.lse)
 
 
+def test_pages_past_4_gib_of_pool(B, D):
+    """The same pages placed at the top of a 5.4 GB pool (byte offsets past
+    2^32, row coordinates past 2^24): bits unchanged, new rows stored there."""
+    w = wl.custom([3000, 777], [[(0, 3000), (100, 2000)], [(0, 777)]], seed=6, n_spare=2)
+    t = wl.materialize(w, "cuda")
+    a = run_resident(D, w, t, False)
+    big = 20480                                    # pages of 256 KiB: 5.37 GB
+    top = np.arange(big - w.pool_pages, big)       # the old pool's pages, in order, at the top
+    pool2 = torch.zeros((1, big) + tuple(t["pool"].shape[2:]), dtype=t["pool"].dtype,
+                        device="cuda")
+    pool2[:, big - w.pool_pages:] = t["pool"]
+    table2 = w.page_table.copy()
+    for r in range(w.batch):
+        n = w.pages_of(r)
+        table2[r, :n] = top[w.page_table[r, :n]]
+    w2 = wl.DecodeWorkload(w.name, w.seed, w.n_layers, w.lengths, w.tiles, table2, big,
+                           top[w.spare_pages], w.geometry)
+    nan = torch.tensor(float("nan"), dtype=pool2.dtype, device="cuda")
+    for r in range(w.batch):                       # the new rows must be stored again
+        pos = int(w.lengths[r]) - 1
+        pool2[0, int(table2[r, pos // 64]), pos % 64] = nan
+    t2 = dict(t)
+    t2["pool"] = pool2
+    t2["page_table"] = torch.as_tensor(table2, device="cuda")
+    b = run_resident(D, w2, t2, False)
+    assert torch.equal(a.o.tile_out, b.o.tile_out) and torch.equal(a.o.tile_lse, b.o.tile_lse)
+    assert torch.equal(a.o.out, b.o.out) and torch.equal(a.o.lse, b.o.lse)
+    for r in range(w.batch):                       # the fused tail write landed up there
+        pos = int(w.lengths[r]) - 1
+        page = int(table2[r, pos // 64])
+        assert page * 262144 > (1 << 32)
+        assert torch.equal(pool2[0, page, pos % 64].view(torch.int16),
+                           t["new_rows"][0, r].view(torch.int16))
+    del pool2, t2
+    torch.cuda.empty_cache()
+
+
 # The tensor-core kernel carries each probability as a bf16 hi + lo pair
 # (relative error <= 2^-18); the CUDA-core kernel keeps fp32.  Their outputs
 # can differ by up to 2^-18 * max|v - out| (~4e-6 * 10 for N(0,1) values), so
