@@ -699,11 +699,26 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
         torch.cuda.synchronize(dev)
         return 3 * seg.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
 
+    # the same one-stream copy over every layer's history (all the host memory
+    # the route stages from): its rate is the route's own ceiling
+    n_seg = host.rows.shape[0] // seg.shape[0]
+
+    def link_probe_all():
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(ps):
+            e0.record(ps)
+            for i in range(n_seg):
+                dst.copy_(host.rows[i * seg.shape[0]:(i + 1) * seg.shape[0]], non_blocking=True)
+            e1.record(ps)
+        torch.cuda.synchronize(dev)
+        return n_seg * seg.numel() * 2 / (e0.elapsed_time(e1) / 1e3) / 1e9
+
     for _ in range(max(3, args.warmup)):
         step()
     st.drain()
     torch.cuda.synchronize(dev)
     probe_before = link_probe()
+    probe_all_before = link_probe_all()
     steps = max(3, min(args.steps, 10))
     t0 = time.perf_counter()
     for _ in range(steps):
@@ -716,6 +731,7 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
     stats = st.handle.stats()
     staged_per_step = stats.staged_bytes // stats.stage_generation * st.stages_per_step()
     probe_after = link_probe()
+    probe_all_after = link_probe_all()
     del dst
     h2d = q_host.numel() * 2 + rows_host.numel() * 2 + staged_per_step
     d2h = out_host.numel() * 4 + lse_host.numel() * 4 + w.n_layers * w.batch * geo.row_bytes
@@ -729,7 +745,10 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
            "ms_per_step": round(1e3 * secs / steps, 3),
            "h2d_GBps": round(staged_per_step * steps / secs / 1e9, 2),
            "link_probe_h2d_GBps": [round(probe_before, 2), round(probe_after, 2)],
-           "link_probe": "one stream, before and after the timed steps",
+           "link_probe_all_layers_h2d_GBps": [round(probe_all_before, 2),
+                                               round(probe_all_after, 2)],
+           "link_probe": "one stream, before and after the timed steps: the first layer's "
+                         "history three times, and every layer's history once",
            "steps": steps, "_secs": secs}
     if compact:
         exact_bytes = sum(run.get("n_rows", 0) * geo.row_bytes
