@@ -260,7 +260,9 @@ def oracle_sample(n_tasks, workers, length=31744):
 
 def cpu_baseline_dict(workers_arg):
     workers = workers_arg or cpu_cores()
-    s = oracle_sample(n_tasks=2 * workers, workers=workers)
+    # one (layer, request) history per worker: ~1.5 s of CPU work each, about
+    # 20-30 s in all on the box's 16 host cores
+    s = oracle_sample(n_tasks=workers, workers=workers)
     gbs = s["kv_bytes"] / s["busy_s"] * workers / 1e9
     return {"value": round(gbs, 4), "unit": UNIT, "cores": workers, "kind": "oracle",
             "sample": (f"{s['tasks']} (layer, request) pairs of 31,744 tokens (4 KV heads x 256, "
