@@ -42,6 +42,7 @@ sys.path.insert(0, ROOT)
 METRIC = "decode-attn KV GB/s (% of HBM peak) and tokens/s at 32K-262K ctx, 1 GB300"
 UNIT = "GB/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_kernel_4x31744.md")
 # the decode kernel's translation unit: the .cu file and the headers it includes
@@ -55,9 +56,15 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", choices=["4x31744", "1x262144", "ragged"], default="4x31744",
+    ap.add_argument("--workload", choices=["4x31744", "1x262144", "ragged", "uniform"],
+                    default="4x31744",
                     help="4x31744 is the benchmarked workload; the others report the same "
-                         "metric for the 262K-token and ragged-window workloads")
+                         "metric for the 262K-token and ragged-window workloads, or for "
+                         "--requests x --ctx tokens in tiles of --tile-tokens (uniform)")
+    ap.add_argument("--requests", type=int, default=1, help="uniform workload: requests")
+    ap.add_argument("--ctx", type=int, default=32768, help="uniform workload: tokens per request")
+    ap.add_argument("--tile-tokens", type=int, default=32768,
+                    help="uniform workload: tokens per tile")
     ap.add_argument("--layers", type=int, default=16,
                     help="layers of the workload (16 is the benchmarked workload; fewer "
                          "layers only make small profiling cases)")
@@ -323,7 +330,9 @@ def run_ours(args):
     from paged_decode_attention_attn_gb300 import workloads as wl
 
     make = {"4x31744": wl.four_requests_31744, "1x262144": wl.one_request_262144,
-            "ragged": wl.ragged_window}[args.workload]
+            "ragged": wl.ragged_window,
+            "uniform": lambda n_layers: wl.uniform(args.requests, args.ctx, args.tile_tokens,
+                                                   n_layers=n_layers)}[args.workload]
     w = make(n_layers=args.layers)
     t = wl.materialize(w, dev)
     geo = w.geometry
@@ -477,7 +486,10 @@ def run_ours(args):
                        "layers": w.n_layers, "heads": "24q/4kv", "head_dim": 256,
                        "page_tokens": 64, "tiles_per_request": w.n_tiles,
                        "route": "resident", "parallelism": f"replicas x{world}",
-                       "l2": f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step)",
+                       "l2": (f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step)"
+                              if kv_bytes > 2 * L2_BYTES else
+                              f"no flush; {kv_bytes / 1e6:.0f} MB of KV per step is within "
+                              "twice the 129 MB L2, so part of it may hit there"),
                        "kernel": "cuda-core fp32" if args.cuda_core
                        else "tensor-core mma.sync bf16 + TMA pipeline"
                        + (", tail write and tile merge fused" if fused else "")

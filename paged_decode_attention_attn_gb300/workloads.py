@@ -150,6 +150,21 @@ def one_request_262144(seed: int = 3, n_layers: int = 16) -> DecodeWorkload:
                           tiles, table, pool_pages, spare)
 
 
+def uniform(batch: int, length: int, tile_tokens: int = 32768, seed: int = 7,
+            n_layers: int = 16) -> DecodeWorkload:
+    """``batch`` requests of ``length`` tokens each, cut into tiles of
+    ``tile_tokens`` (the last one ragged), pages shuffled in a pool with 16
+    NaN spare pages: the bench's other shapes."""
+    if batch < 1 or length < 1 or tile_tokens < 1:
+        raise ValueError("batch, length and tile_tokens must be >= 1")
+    rng = np.random.default_rng(seed)
+    lengths = np.full(batch, length, dtype=np.int64)
+    table, pool_pages, spare = _shuffled_tables(rng, lengths, -(-length // PAGE_TOKENS), 16)
+    tiles = _pad_tiles([_split_tiles(0, length, tile_tokens)] * batch)
+    return DecodeWorkload(f"{batch}x{length}-{n_layers}layers-{tiles.shape[1]}tiles", seed,
+                          n_layers, lengths, tiles, table, pool_pages, spare)
+
+
 def window_tiles(length: int, sink_pages: int = 1, recent_pages: int = 64,
                  tile_tokens: int = 32768, page_tokens: int = PAGE_TOKENS):
     """Tiles of a request whose sink page and newest pages stay resident.
