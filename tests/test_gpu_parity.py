@@ -331,3 +331,62 @@ def test_other_head_geometries_match_oracle(B, D, hq, hkv):
         o = fused.o
         assert_close_to_oracle(o.tile_out[0, r], o.tile_lse[0, r], o.out[0, r], o.lse[0, r],
                                ref, w.tiles[r], f"{hq}q/{hkv}kv request {r}")
+
+
+def split_counts(lengths, tiles, n_kv_heads, sms, charge=6, page=64):
+    """CTAs covering each (request, tile, kv head) unit when a launch's pages,
+    each non-empty unit preceded by `charge` pages of bookkeeping, are cut
+    into `sms` equal shares (the decode launch's work split)."""
+    units = [(s, e) for _ in range(n_kv_heads) for tl in tiles for (s, e) in tl]
+    spans, total = [], 0
+    for s, e in units:
+        n = -(-e // page) - s // page if e > s else 0
+        if n:
+            total += charge
+            spans.append((total, n))
+        total += n
+    grid = min(sms, total)
+    cta = lambda p: ((p + 1) * grid - 1) // total
+    return [cta(f + n - 1) - cta(f) + 1 for f, n in spans]
+
+
+@pytest.mark.parametrize("cuda_core", VARIANTS, ids=VARIANT_IDS)
+@pytest.mark.parametrize("batch", [1, 2, 3])
+def test_units_split_over_many_ctas(B, D, cuda_core, batch):
+    """One tile per request of a few thousand tokens spreads each (request,
+    kv head) unit over 11-36 CTAs, whose partials the last of them merges
+    (more than one register batch of partials, and more than one warp's
+    worth of statistics).  The result must match the oracle, agree with the
+    same history cut into two tiles and merged, and keep its bits when the
+    pages move."""
+    rng = np.random.default_rng(40 + batch)
+    lengths = [int(x) for x in rng.integers(2500, 9000, size=batch)]
+    one = [[(0, L)] for L in lengths]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    counts = split_counts(lengths, one, 4, sms)
+    assert max(counts) >= 13, counts
+    w = wl.custom(lengths, one, seed=60 + batch, n_spare=3)
+    t = wl.materialize(w, "cuda")
+    a = run_resident(D, w, t, cuda_core)
+    cut = [[(0, L // 3), (L // 3, L)] for L in lengths]
+    b = run_resident(D, w, t, cuda_core, tiles=wl._pad_tiles([list(c) for c in cut]))
+    for r in range(batch):
+        ref = oracle_request(w, t, 0, r)
+        assert_close_to_oracle(a.o.tile_out[0, r], a.o.tile_lse[0, r], a.o.out[0, r],
+                               a.o.lse[0, r], ref, w.tiles[r], f"request {r} of {batch}")
+        assert max_abs(b.o.out[0, r].cpu(), a.o.tile_out[0, r, 0].cpu()) <= TOL_SPLIT
+        assert max_abs(b.o.lse[0, r].cpu(), a.o.tile_lse[0, r, 0].cpu()) <= TOL_SPLIT
+    # placement: reverse the physical order of the pool's pages
+    perm = np.arange(w.pool_pages)[::-1].copy()
+    pool2 = torch.empty_like(t["pool"])
+    pool2[:, torch.as_tensor(perm, device="cuda")] = t["pool"]
+    table2 = w.page_table.copy()
+    for r in range(batch):
+        n = w.pages_of(r)
+        table2[r, :n] = perm[w.page_table[r, :n]]
+    w2 = wl.DecodeWorkload(w.name, w.seed, w.n_layers, w.lengths, w.tiles, table2,
+                           w.pool_pages, perm[w.spare_pages], w.geometry)
+    t2 = dict(t, pool=pool2, page_table=torch.as_tensor(table2, device="cuda"))
+    c = run_resident(D, w2, t2, cuda_core)
+    assert torch.equal(a.o.tile_out, c.o.tile_out) and torch.equal(a.o.tile_lse, c.o.tile_lse)
+    assert torch.equal(a.o.out, c.o.out) and torch.equal(a.o.lse, c.o.lse)
