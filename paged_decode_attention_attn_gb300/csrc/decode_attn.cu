@@ -874,11 +874,16 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         const float2* pml = reinterpret_cast<const float2*>(p.part_ml) +
                             (size_t)U.part_base * kMaxG;
         for (int row = warp; row < G; row += kConsumerWarps) {
-          const float2 first =
-              lane < n ? __ldcg(pml + (size_t)lane * kMaxG + row) : make_float2(-INFINITY, 0.f);
-          float big_m = first.x;
-          int nan = (first.x != first.x);
-          for (int c = lane + 32; c < n; c += 32) {
+          // Lanes hold the statistics of partials lane and lane + 32 in
+          // registers (one round trip up to 64 partials); beyond that they
+          // are read again for the weights.
+          const float2 none = make_float2(-INFINITY, 0.f);
+          const float2 first = lane < n ? __ldcg(pml + (size_t)lane * kMaxG + row) : none;
+          const float2 second =
+              lane + 32 < n ? __ldcg(pml + (size_t)(lane + 32) * kMaxG + row) : none;
+          float big_m = fmaxf(first.x, second.x);
+          int nan = (first.x != first.x) | (second.x != second.x);
+          for (int c = lane + 64; c < n; c += 32) {
             const float mc = __ldcg(pml + (size_t)c * kMaxG + row).x;
             nan |= (mc != mc);
             big_m = fmaxf(big_m, mc);
@@ -894,7 +899,12 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
             wts[lane * kMaxG + row] = a;
             l = a * first.y;
           }
-          for (int c = lane + 32; c < n; c += 32) {
+          if (lane + 32 < n) {
+            const float a = ref_weight(second.x, big_m);
+            wts[(lane + 32) * kMaxG + row] = a;
+            l = fmaf(a, second.y, l);
+          }
+          for (int c = lane + 64; c < n; c += 32) {
             const float2 ml = __ldcg(pml + (size_t)c * kMaxG + row);
             const float a = ref_weight(ml.x, big_m);
             wts[c * kMaxG + row] = a;

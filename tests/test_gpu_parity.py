@@ -350,22 +350,27 @@ def split_counts(lengths, tiles, n_kv_heads, sms, charge=6, page=64):
     return [cta(f + n - 1) - cta(f) + 1 for f, n in spans]
 
 
+SPLIT_CASES = [(1, 24, 4), (2, 24, 4), (3, 24, 4), (1, 8, 1)]   # (requests, hq, hkv)
+
+
 @pytest.mark.parametrize("cuda_core", VARIANTS, ids=VARIANT_IDS)
-@pytest.mark.parametrize("batch", [1, 2, 3])
-def test_units_split_over_many_ctas(B, D, cuda_core, batch):
+@pytest.mark.parametrize("batch,hq,hkv", SPLIT_CASES,
+                         ids=[f"{b}x-{q}q{k}kv" for b, q, k in SPLIT_CASES])
+def test_units_split_over_many_ctas(B, D, cuda_core, batch, hq, hkv):
     """One tile per request of a few thousand tokens spreads each (request,
-    kv head) unit over 11-36 CTAs, whose partials the last of them merges
-    (more than one register batch of partials, and more than one warp's
-    worth of statistics).  The result must match the oracle, agree with the
-    same history cut into two tiles and merged, and keep its bits when the
-    pages move."""
+    kv head) unit over 11-36 CTAs (107 with one kv head), whose partials the
+    last of them merges: more than one register batch of partials, and more
+    than one and more than two warps' worth of statistics.  The result must
+    match the oracle, agree with the same history cut into two tiles and
+    merged, and keep its bits when the pages move."""
     rng = np.random.default_rng(40 + batch)
     lengths = [int(x) for x in rng.integers(2500, 9000, size=batch)]
     one = [[(0, L)] for L in lengths]
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    counts = split_counts(lengths, one, 4, sms)
+    counts = split_counts(lengths, one, hkv, sms)
     assert max(counts) >= 13, counts
-    w = wl.custom(lengths, one, seed=60 + batch, n_spare=3)
+    geo = wl.Geometry(n_q_heads=hq, n_kv_heads=hkv)
+    w = wl.custom(lengths, one, seed=60 + batch, n_spare=3, geometry=geo)
     t = wl.materialize(w, "cuda")
     a = run_resident(D, w, t, cuda_core)
     cut = [[(0, L // 3), (L // 3, L)] for L in lengths]
