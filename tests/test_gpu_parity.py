@@ -256,9 +256,9 @@ def test_lse_merge_stress_matches_unsplit_softmax(B):
 
 @pytest.mark.parametrize("D", [4, 12, 128, 132, 256, 260, 520])
 def test_lse_merge_head_dims_and_partial_counts(B, D):
-    """Rows of any width (one or several 128-column warps, a ragged last one)
-    and partial counts on both sides of the load batch, against the oracle's
-    fp64 merge of the same fp32 partials."""
+    """Rows of any width (one or several 64-column passes, a ragged last one)
+    and partial counts on both sides of the kernel's eight-partial stages,
+    against the oracle's fp64 merge of the same fp32 partials."""
     dev = "cuda"
     g = torch.Generator(device=dev).manual_seed(D)
     H = 3
