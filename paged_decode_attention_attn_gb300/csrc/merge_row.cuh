@@ -1,6 +1,7 @@
-// The FP32 log-sum-exp merge of one (request, head) row, shared by the merge
-// kernel and the decode kernel's fused cross-tile merge so that both give the
-// same bits.
+// The FP32 log-sum-exp merge of one (request, head) row, used by the decode
+// kernel's fused cross-tile merge.  The standalone merge kernel (lse_merge.cu)
+// computes every column with the same expressions in the same partial order,
+// so both give the same bits.
 //
 // Merge rule ("KV-cache engineering", section "Exact recent pages, compact
 // older pages"): weight each partial by exp(LSE_i - max LSE), sum the weighted
