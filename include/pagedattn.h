@@ -179,11 +179,14 @@ int paged_decode_attn_lse_cuda_core(const void* q, const void* pool, int64_t poo
  *   All arguments as for paged_decode_attn_lse, except:
  *   status  optional device int32; receives the call's PA_STATUS_* bits (the
  *           copy is enqueued on the stream after the kernel), or NULL.
- * Returns PA_ERR_INVALID, before touching the GPU, when the call would need
- * more scratch than the array holds (above ~1,000 (request, tile, kv head)
- * units); paged_decode_attn_lse with a caller workspace has no such limit.
- * The first call on each device looks up the array's device address with
- * that device current; make that first call before any stream capture.  Every
+ * Every argument is checked before the GPU is touched: a refused call
+ * enqueues nothing and leaves the array as it was.  Returns PA_ERR_INVALID
+ * when the call would need more scratch than the array holds (above ~1,000
+ * (request, tile, kv head) units); paged_decode_attn_lse with a caller
+ * workspace has no such limit.  The first call in each device's context
+ * looks up the array's device address with that device current (and looks
+ * it up again if the context is later destroyed and made anew, as after
+ * cudaDeviceReset); make that first call before any stream capture.  Every
  * call clears the start of the array and reuses the rest, so calls whose
  * kernels may overlap on the GPU (unordered streams) race and must not be
  * issued. */
@@ -263,7 +266,10 @@ int paged_decode_attn_test_stall(int iteration, uint64_t wait_limit_ns);
  *   out_parts    device fp32 [n_parts][H][D];  lse_parts device fp32 [n_parts][H]
  *   part_offsets device int32 [B+1], non-decreasing, part_offsets[0] = 0.
  *   out, lse     device fp32 [B][H][D], [B][H].
- * D must be a positive multiple of 4 and the fp32 arrays 16-byte aligned. */
+ * D must be a positive multiple of 4 and the fp32 arrays 16-byte aligned.
+ * Every pointer must be non-NULL whenever B * H > 0 (PA_ERR_INVALID
+ * otherwise), out_parts and lse_parts included: the offsets are on the
+ * device, so the call cannot know that no partial will be read. */
 int lse_merge(const float* out_parts, const float* lse_parts,
               const int32_t* part_offsets, int B, int H, int D,
               float* out, float* lse, cudaStream_t stream);

@@ -1074,13 +1074,13 @@ int launch_units(const CUtensorMap& tmap, const std::vector<Unit>& units, size_t
 thread_local int t_stall_iteration = -1;
 thread_local unsigned long long t_wait_limit_ns = 0;
 
-int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
-        const int32_t* page_table, int max_pages, const int32_t* tiles, int B, int T,
-        int n_q_heads, int n_kv_heads, int head_dim, float scale, float* out, float* lse,
-        void* workspace, size_t ws_bytes, cudaStream_t stream,
-        const int32_t* positions = nullptr, const void* new_rows = nullptr,
-        unsigned flags = 0, float* merged_out = nullptr, float* merged_lse = nullptr) {
-  clear_error();
+// Every host-side check of a decode call; enqueues nothing and touches no
+// device state.  B * T == 0 passes (the call is then a no-op).
+int check_args(const void* q, const void* pool, int64_t pool_pages, const int32_t* page_table,
+               int max_pages, const int32_t* tiles, int B, int T, int n_q_heads,
+               int n_kv_heads, int head_dim, float* out, float* lse, const void* workspace,
+               size_t ws_bytes, const int32_t* positions, const void* new_rows, unsigned flags,
+               const float* merged_out, const float* merged_lse) {
   PA_REQUIRE(B >= 0 && T >= 0, "B and T must be >= 0 (got %d, %d)", B, T);
   if ((long long)B * T == 0) return PA_OK;
   if (head_dim != kD)
@@ -1120,6 +1120,21 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
              "positions and new_rows go together");
   PA_REQUIRE(new_rows == nullptr || reinterpret_cast<uintptr_t>(new_rows) % 16 == 0,
              "new_rows must be 16-byte aligned");
+  return PA_OK;
+}
+
+int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
+        const int32_t* page_table, int max_pages, const int32_t* tiles, int B, int T,
+        int n_q_heads, int n_kv_heads, int head_dim, float scale, float* out, float* lse,
+        void* workspace, size_t ws_bytes, cudaStream_t stream,
+        const int32_t* positions = nullptr, const void* new_rows = nullptr,
+        unsigned flags = 0, float* merged_out = nullptr, float* merged_lse = nullptr) {
+  clear_error();
+  int rc0 = check_args(q, pool, pool_pages, page_table, max_pages, tiles, B, T, n_q_heads,
+                       n_kv_heads, head_dim, out, lse, workspace, ws_bytes, positions, new_rows,
+                       flags, merged_out, merged_lse);
+  if (rc0 != PA_OK || (long long)B * T == 0) return rc0;
+  const int G = n_q_heads / n_kv_heads;
   EncodeTiledFn enc = encode_fn();
   if (!enc) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
 
@@ -1316,27 +1331,74 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[64] = {nullptr};
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on the current device.  The host-side
-// name of the array is not a device address; the runtime is asked for it once
-// per device, with that device current.
+// Id of the CUDA context current on this thread (unique for the process's
+// lifetime, so a context destroyed and made again gets a new one); false if
+// no context is current or the driver cannot say.
+bool current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(ptr);
+    ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(ptr);
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+  return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+struct ScratchAddress {
+  unsigned long long ctx_id = 0;
+  void* ptr = nullptr;
+};
+
+std::mutex g_noalloc_mu;
+ScratchAddress g_noalloc_addr[64];
+
+// Device address of the scratch array in the current device's context.  The
+// host-side name of the array is not a device address, and the address the
+// runtime gives is valid only in the context it was looked up in (a device
+// reset, or a primary context released and made again, loads the module
+// anew, possibly elsewhere).  So the address is kept per device together
+// with the id of the context it came from, and looked up again, with that
+// device current, whenever the current context is another one.  If the
+// driver cannot name the current context, every call looks it up.
 int noalloc_scratch(void** out) {
   int dev = 0;
   const cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return pa::fail(PA_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= 64) return pa::fail(PA_ERR_INVALID, "device index %d out of range", dev);
+  unsigned long long id = 0;
+  bool have_id = current_context_id(&id);
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (g_noalloc_ptr[dev] == nullptr) {
+  ScratchAddress& c = g_noalloc_addr[dev];
+  if (!have_id || c.ptr == nullptr || c.ctx_id != id) {
     void* ptr = nullptr;
     const cudaError_t r = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
     if (r != cudaSuccess || ptr == nullptr)
       return pa::fail(PA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s",
                       cudaGetErrorString(r));
-    g_noalloc_ptr[dev] = ptr;
+    // The lookup makes the device's primary context current if none was.
+    if (!have_id) have_id = current_context_id(&id);
+    c.ptr = have_id ? ptr : nullptr;
+    c.ctx_id = have_id ? id : 0;
+    *out = ptr;
+    return PA_OK;
   }
-  *out = g_noalloc_ptr[dev];
+  *out = c.ptr;
   return PA_OK;
 }
 
@@ -1353,14 +1415,24 @@ extern "C" int paged_decode_attn_lse_noalloc(const void* q, const void* pool, in
   if ((long long)B * T == 0) return PA_OK;
   const size_t need =
       paged_decode_attn_lse_workspace_bytes(B, T, n_q_heads, n_kv_heads, head_dim);
-  if (need > kNoAllocScratchBytes)
+  if (need == 0) {
+    // An unsupported geometry: let the checks below name it.
+  } else if (need > kNoAllocScratchBytes)
     return pa::fail(PA_ERR_INVALID,
                     "this call needs %zu bytes of scratch, more than the %zu bytes the "
                     "no-allocation entry point holds; pass a workspace to "
                     "paged_decode_attn_lse instead",
                     need, kNoAllocScratchBytes);
+  // Every argument is checked before the scratch is looked up or cleared,
+  // so a refused call leaves the GPU and the array untouched.  The check
+  // sees a stand-in workspace pointer (never dereferenced) of the array's size.
+  int rc = pa::decode::check_args(q, pool, pool_pages, page_table, max_pages, tiles, B, T,
+                                  n_q_heads, n_kv_heads, head_dim, out, lse,
+                                  reinterpret_cast<const void*>(uintptr_t(256)),
+                                  kNoAllocScratchBytes, nullptr, nullptr, 0, nullptr, nullptr);
+  if (rc != PA_OK) return rc;
   void* scratch = nullptr;
-  int rc = noalloc_scratch(&scratch);
+  rc = noalloc_scratch(&scratch);
   if (rc != PA_OK) return rc;
   // Status word and arrival counters must start at zero.
   const cudaError_t e = cudaMemsetAsync(scratch, 0, pa::decode::kStatusBytes + pa::decode::kCounterBytes,

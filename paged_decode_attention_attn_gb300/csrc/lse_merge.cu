@@ -195,7 +195,9 @@ extern "C" int lse_merge(const float* out_parts, const float* lse_parts,
   pa::clear_error();
   PA_REQUIRE(B >= 0 && H >= 0 && D >= 0, "negative size");
   if ((long long)B * H == 0) return PA_OK;
-  PA_REQUIRE(part_offsets && out && lse, "null pointer argument");
+  // The partial arrays are required even when every request may turn out to
+  // have none: the offsets live on the device, so the host cannot tell.
+  PA_REQUIRE(out_parts && lse_parts && part_offsets && out && lse, "null pointer argument");
   PA_REQUIRE(D > 0 && D % 4 == 0, "D (%d) must be a positive multiple of 4", D);
   PA_REQUIRE(reinterpret_cast<uintptr_t>(out) % 16 == 0 &&
                  reinterpret_cast<uintptr_t>(out_parts) % 16 == 0,

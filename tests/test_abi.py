@@ -86,11 +86,38 @@ def test_decode_argument_checks(B):
                                        0, 0, 0, None) == B.PA_OK
 
 
+def test_noalloc_refuses_before_touching_the_gpu(B):
+    """The allocation-free decode entry point checks every argument before it
+    looks up or clears its scratch array: on a machine without a GPU these
+    calls fail with the argument's own error, not with a CUDA error."""
+    fake = 1 << 20
+    ok = np.ascontiguousarray(np.asarray([[[0, 64]]], dtype=np.int32))
+
+    def call(q=fake, tiles=ok, nq=24, nkv=4, head_dim=256, out=fake, max_pages=8):
+        return B.lib.paged_decode_attn_lse_noalloc(q, fake, 16, fake, max_pages,
+                                                   tiles.ctypes.data, tiles.shape[0],
+                                                   tiles.shape[1], nq, nkv, head_dim, 0.0625,
+                                                   out, fake, None, None)
+    assert call(head_dim=128) == B.PA_ERR_UNSUPPORTED
+    assert call(nq=72) == B.PA_ERR_UNSUPPORTED
+    assert call(nq=25) == B.PA_ERR_INVALID
+    assert call(q=None) == B.PA_ERR_INVALID
+    assert call(q=fake + 8) == B.PA_ERR_INVALID
+    assert "q must be 16-byte aligned" in B.last_error()
+    assert call(out=fake + 4) == B.PA_ERR_INVALID
+    bad = np.ascontiguousarray(np.asarray([[[0, 9 * 64]]], dtype=np.int32))
+    assert call(tiles=bad) == B.PA_ERR_INVALID                       # past the table
+    assert "outside" in B.last_error()
+
+
 def test_merge_and_append_argument_checks(B):
     fake = 1 << 20
     assert B.lib.lse_merge(fake, fake, fake, 2, 24, 254, fake, fake, None) == B.PA_ERR_INVALID
     assert B.lib.lse_merge(fake, fake, fake, 0, 24, 256, fake, fake, None) == B.PA_OK
     assert B.lib.lse_merge(fake, fake, fake, 2, 24, 0, fake, fake, None) == B.PA_ERR_INVALID
+    # the partial arrays are required whenever there are rows to merge
+    assert B.lib.lse_merge(None, fake, fake, 2, 24, 256, fake, fake, None) == B.PA_ERR_INVALID
+    assert B.lib.lse_merge(fake, None, fake, 2, 24, 256, fake, fake, None) == B.PA_ERR_INVALID
     assert B.lib.kv_append_rows(fake, 4, fake, 4, fake, fake, 1, 4008, None, None) == \
         B.PA_ERR_INVALID
     assert B.lib.kv_append_rows(fake, 4, fake, 4, fake, fake + 8, 1, 4096, None, None) == \
