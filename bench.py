@@ -1,22 +1,34 @@
 """Decode-attention benchmark: KV GB/s and tokens/s of one decode step.
 
-Workload: 4 requests x 31,744-token histories, 16 layers, 24 query / 4 KV heads,
-head_dim 256, bf16 K/V in 64-token pages (4,096 B per token per layer), one
-32K tile per request, FP32 LSE merge.  A step is, for all 16 layers: write the
-new token's row into its page, paged GQA decode attention with per-tile LSE,
-LSE merge.
+Headline workload: 4 requests x 31,744-token histories, 16 layers, 24 query /
+4 KV heads, head_dim 256, bf16 K/V in 64-token pages (4,096 B per token per
+layer), one 32K tile per request, FP32 LSE merge.  A step is, for all 16
+layers: write the new token's row into its page, paged GQA decode attention
+with per-tile LSE, LSE merge.
 
   value  resident route: history already in HBM; KV GB/s = sum_r L_r x 4,096 B
          x 16 layers per step / step time.
   e2e    host-staged route through the same C-ABI with host buffers: per step
          Q and the new rows go host->device, every layer's history is staged
          from pinned host memory into a 2-slot device arena, the tail rows are
-         written back, and the outputs come back to the host.
+         written back, and the outputs come back to the host.  Each staged leg
+         carries a per-stage timeline (copy time and rate, idle time of the
+         H2D stream waiting for the host or for a slot, compute-stream waits)
+         from CUDA events in its timed region, and route/probe pairs: single
+         steps alternated with a one-stream copy of the same host memory.
   e2e_resident  the resident route through the same calls with host buffers:
          history in HBM, per step Q and new rows in, merged outputs out.
   roofline  the attention kernel alone: algorithmic bytes per launch / mean
          launch time (CUDA events on the launching stream), against the
          measured HBM copy bandwidth.
+  workloads  the same resident value, roofline and staged e2e for the other
+         workloads of the metric's 32K-262K range: 1 x 262,144 tokens in 8
+         tiles, 8 ragged requests of 8K-128K tokens with a sink + newest-64
+         resident window, and a single 32,768-token request.
+  bus_model  the staged step's latency model t = fixed + bytes / bandwidth,
+         fitted on the median single-step time of 1 request at 32K, 64K, 128K
+         and 262K tokens, with its worst error there and its prediction of
+         every staged leg's median single step.
   cpu_baseline  the fp64 NumPy oracle on a bounded sample on the host cores.
   merge_stress  the standalone FP32 LSE merge on 64 requests x 24 heads x 256
          with 1..64 partials each: GB/s of partials read and rows written.
@@ -44,7 +56,6 @@ UNIT = "GB/s"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "paged_decode_kernel_4x31744.md")
 # the decode kernel's translation unit: the .cu file and the headers it includes
 KERNEL_SOURCES = [os.path.join(ROOT, "paged_decode_attention_attn_gb300", "csrc", f)
                   for f in ("decode_attn.cu", "merge_row.cuh", "ptx.cuh", "common.h")] + [
@@ -83,6 +94,12 @@ def parse_args(argv=None):
     ap.add_argument("--no-merge-arm", action="store_true",
                     help="skip the standalone LSE-merge measurement on the merge-stress shape")
     ap.add_argument("--cpu-workers", type=int, default=0)
+    ap.add_argument("--no-extra-workloads", action="store_true",
+                    help="report only the --workload workload (no 'workloads' key)")
+    ap.add_argument("--no-bus-model-leg", action="store_true",
+                    help="leave the fitted bus model out of the bench line")
+    ap.add_argument("--ab-pairs", type=int, default=5,
+                    help="route/probe pairs per staged leg")
     ap.add_argument("--bus-model", action="store_true",
                     help="fit the staged route's latency model over 32K-262K tokens "
                          "(prints its own JSON line instead of the bench line)")
@@ -133,7 +150,7 @@ def whole_job_gbs(bytes_per_step_per_rank, steps, max_ms, world):
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi in loop mode (every 100 ms) for the duration of the region."""
+    """nvidia-smi in loop mode (every 50 ms) for the duration of the region."""
 
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -147,7 +164,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -193,17 +210,26 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def recorded_traffic():
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the kernel's sources as they are now (sha256 over the files of
-    KERNEL_SOURCES in order), else None."""
+def traffic_file(workload):
+    return os.path.join(ROOT, "profiles", f"paged_decode_kernel_{workload}.md")
+
+
+def kernel_source_sha():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
+def recorded_traffic(workload="4x31744", n_layers=16):
+    """DRAM bytes per launch of the workload's full launch, from the committed
+    ncu summary, if it was taken on the kernel's sources as they are now
+    (sha256 over the files of KERNEL_SOURCES in order) and the bench runs the
+    workload's layer count; else None."""
     try:
-        h = hashlib.sha256()
-        for f in KERNEL_SOURCES:
-            h.update(open(f, "rb").read())
-        src = h.hexdigest()
+        src = kernel_source_sha()
         fields = {}
-        for line in open(TRAFFIC_FILE):
+        for line in open(traffic_file(workload)):
             if ":" in line and line.strip().startswith("- "):
                 k, v = line.strip()[2:].split(":", 1)
                 fields[k.strip()] = v.strip().strip("`")
@@ -319,33 +345,34 @@ def run_reference(args, budget_s=150.0):
 # GPU arm
 # ---------------------------------------------------------------------------
 
-def run_ours(args):
-    import numpy as np
-    import torch
-    rank, world, local = dist_init(args.gpus)
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    from paged_decode_attention_attn_gb300 import binding as B
-    from paged_decode_attention_attn_gb300 import decode as D
-    from paged_decode_attention_attn_gb300 import workloads as wl
+EXTRA_WORKLOADS = ("1x262144", "ragged", "1x32768")
 
-    make = {"4x31744": wl.four_requests_31744, "1x262144": wl.one_request_262144,
-            "ragged": wl.ragged_window,
-            "uniform": lambda n_layers: wl.uniform(args.requests, args.ctx, args.tile_tokens,
-                                                   n_layers=n_layers)}[args.workload]
-    w = make(n_layers=args.layers)
-    t = wl.materialize(w, dev)
+
+def make_workload(name, args, n_layers):
+    from paged_decode_attention_attn_gb300 import workloads as wl
+    if name == "4x31744":
+        return wl.four_requests_31744(n_layers=n_layers)
+    if name == "1x262144":
+        return wl.one_request_262144(n_layers=n_layers)
+    if name == "ragged":
+        return wl.ragged_window(n_layers=n_layers)
+    if name == "1x32768":
+        return wl.uniform(1, 32768, 32768, n_layers=n_layers)
+    return wl.uniform(args.requests, args.ctx, args.tile_tokens, n_layers=n_layers)
+
+
+def resident_leg(args, w, t, dev, D, B, world, steps):
+    """The resident route of one workload: the 16 launches of a step captured
+    in a CUDA graph and replayed ``steps`` times between a barrier and a
+    synchronize (the timed region), then the same steps run eagerly with CUDA
+    events around every launch."""
+    import torch
     geo = w.geometry
-    kv_bytes = w.kv_bytes_per_step()
-    kv_bytes_layer = kv_bytes // w.n_layers
     stream = torch.cuda.current_stream(dev)
     res = D.ResidentDecode(w, t, cuda_core=args.cuda_core, stream=stream)
-
-    # ---- resident route: value (CUDA-graph replay of the whole step) ----
-    n_ev = args.steps * w.n_layers
+    n_ev = steps * w.n_layers
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(n_ev)]
-
     fused = not (args.cuda_core or args.unfused)
     # Within the step the pool and page table are written only by the step's
     # own fused launches (layer i's launch stores layer i's new row), so each
@@ -395,80 +422,177 @@ def run_ours(args):
         graph.replay()
     torch.cuda.synchronize(dev)
 
-    clocks = ClockSampler(local)
-    clocks.start()
     barrier(world)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
     host_t0 = time.perf_counter()
-    for _ in range(args.steps):
+    for _ in range(steps):
         graph.replay()
     host_issue_s = time.perf_counter() - host_t0
     end.record(stream)
     torch.cuda.synchronize(dev)
     barrier(world)
     elapsed_ms = start.elapsed_time(end)
-    # ---- roofline of the attention kernel: events around every launch of an
-    # eager run of the same steps (a second timed region, same clocks record) ----
-    for k in range(args.steps):
+    # ---- per-launch events of an eager run of the same steps ----
+    for k in range(steps):
         resident_step(k, stream)
     torch.cuda.synchronize(dev)
-    clk = clocks.stop()
     kernel_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     status = res.kernel_status()
     if status != 0:
-        raise RuntimeError(f"kernel status word {status:#x}")
-    max_ms = max_over_ranks(elapsed_ms, world)
-    step_ms = max_ms / args.steps
-    value = whole_job_gbs(kv_bytes, args.steps, max_ms, world)
-    tokens_per_s = world * w.batch * args.steps / (max_ms / 1e3)
-    peak, peak_kind = hbm_peak()
-    eager_ms = statistics.mean(kernel_ms)
-    if launches_per_step == w.n_layers:
+        raise RuntimeError(f"{w.name}: kernel status word {status:#x}")
+    return dict(res=res, graph=graph, elapsed_ms=elapsed_ms, host_issue_s=host_issue_s,
+                kernel_ms=kernel_ms, launches_per_step=launches_per_step, fused=fused,
+                kv_ready=kv_ready, steps=steps)
+
+
+def resident_summary(args, name, w, leg, world, peak, peak_kind):
+    """value, tokens/s and the kernel roofline of one resident leg."""
+    steps = leg["steps"]
+    kv_bytes = w.kv_bytes_per_step()
+    kv_bytes_layer = kv_bytes // w.n_layers
+    max_ms = max_over_ranks(leg["elapsed_ms"], world)
+    value = whole_job_gbs(kv_bytes, steps, max_ms, world)
+    eager_ms = statistics.mean(leg["kernel_ms"])
+    if leg["launches_per_step"] == w.n_layers:
         # The timed region holds nothing but this kernel's launches (one per
         # layer), so its CUDA-event time over the launches is the kernel's
         # average launch duration as the step runs it (back to back, under
         # programmatic dependent launch).
-        kern_ms = elapsed_ms / (args.steps * w.n_layers)
+        kern_ms = leg["elapsed_ms"] / (steps * w.n_layers)
         kern_how = "timed region / launches (the region holds only this kernel)"
     else:
         kern_ms = eager_ms
         kern_how = "events around each launch of an eager run of the same steps"
     achieved = kv_bytes_layer / (kern_ms / 1e3) / 1e9
+    traffic = recorded_traffic(name)
+    return {
+        "value": round(value, 2), "unit": UNIT, "ms_per_step": round(max_ms / steps, 4),
+        "tokens_per_s": round(world * w.batch * steps / (max_ms / 1e3), 1),
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "kv_bytes_per_step": int(kv_bytes), "steps": steps,
+        "host_issue_ms_per_step": round(1e3 * leg["host_issue_s"] / steps, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "frac_of_nominal_8000": round(achieved / 8000.0, 4),
+                     "traffic": traffic,
+                     "kernel": "paged_decode_kernel",
+                     "bytes_per_launch": kv_bytes_layer,
+                     "mean_launch_ms": round(kern_ms, 5),
+                     "launch_ms_from": kern_how,
+                     "eager_launch_ms": round(eager_ms, 5)},
+    }
+
+
+def workload_config(w, world, fused, kv_ready, args):
+    kv_bytes = w.kv_bytes_per_step()
+    return {"workload": w.name, "batch": w.batch,
+            "ctx": int(w.lengths[0]) if w.batch == 1 or len(set(w.lengths)) == 1
+            else [int(x) for x in w.lengths],
+            "layers": w.n_layers, "heads": "24q/4kv", "head_dim": 256,
+            "page_tokens": 64, "tiles_per_request": w.n_tiles,
+            "route": "resident", "parallelism": f"replicas x{world}",
+            "l2": (f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step)"
+                   if kv_bytes > 2 * L2_BYTES else
+                   f"no flush; {kv_bytes / 1e6:.0f} MB of KV per step is within "
+                   "twice the 129 MB L2, so part of it may hit there"),
+            "kernel": "cuda-core fp32" if args.cuda_core
+            else "tensor-core mma.sync bf16 + TMA pipeline"
+            + (", tail write and tile merge fused" if fused else "")
+            + (", early page loads" if kv_ready else ""),
+            "accumulate": "fp32"}
+
+
+def finish_e2e(e2e, kv_bytes, world):
+    """Whole-job value of a staged or resident e2e leg: every rank's bytes
+    over the slowest rank's wall time."""
+    secs = max_over_ranks(e2e.pop("_secs"), world)
+    e2e["value"] = round(whole_job_gbs(kv_bytes, e2e["steps"], secs * 1e3, world), 2)
+    e2e["ms_per_step"] = round(1e3 * secs / e2e["steps"], 3)
+    return e2e
+
+
+def run_ours(args):
+    import torch
+    rank, world, local = dist_init(args.gpus)
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from paged_decode_attention_attn_gb300 import binding as B
+    from paged_decode_attention_attn_gb300 import decode as D
+    from paged_decode_attention_attn_gb300 import workloads as wl  # noqa: F401
+
+    peak, peak_kind = hbm_peak()
+    names = [args.workload]
+    if not args.no_extra_workloads:
+        names += [n for n in EXTRA_WORKLOADS if n != args.workload]
+    wls, ts = {}, {}
+    for name in names:
+        wls[name] = make_workload(name, args, args.layers)
+        ts[name] = wl.materialize(wls[name], dev)
+    w, t = wls[args.workload], ts[args.workload]
+
+    # ---- resident route of every workload; clocks sampled from the start of
+    # the headline's timed region to the end of the last workload's ----
+    clocks = ClockSampler(local)
+    legs = {}
+    clocks.start()
+    for name in names:
+        legs[name] = resident_leg(args, wls[name], ts[name], dev, D, B, world, args.steps)
+    clk = clocks.stop()
+    clk["window"] = ("the resident timed regions (and per-launch eager runs) of every "
+                     "workload, headline first")
+    summaries = {n: resident_summary(args, n, wls[n], legs[n], world, peak, peak_kind)
+                 for n in names}
+    head = summaries[args.workload]
+    leg = legs[args.workload]
+    fused, kv_ready = leg["fused"], leg["kv_ready"]
     null_ms = null_arm(args, w, t, D, B, dev, fused, kv_ready)
     merge_stress = None if args.no_merge_arm else merge_arm(dev, B)
     e2e_resident = None
     if not args.no_e2e:
-        e2e_resident = run_e2e_resident(args, w, t, res.o, graph, dev)
-        secs = max_over_ranks(e2e_resident.pop("_secs"), world)
-        e2e_resident["value"] = round(whole_job_gbs(kv_bytes, e2e_resident["steps"], secs * 1e3,
-                                                    world), 2)
-        e2e_resident["ms_per_step"] = round(1e3 * secs / e2e_resident["steps"], 4)
-        if res.kernel_status() != 0:
+        e2e_resident = finish_e2e(run_e2e_resident(args, w, t, leg["res"].o, leg["graph"], dev),
+                                  w.kv_bytes_per_step(), world)
+        if leg["res"].kernel_status() != 0:
             raise RuntimeError("kernel status non-zero after the resident e2e steps")
+    for n in names:          # graphs and workspaces of the resident legs
+        legs[n] = None
+    torch.cuda.empty_cache()
 
-    # ---- staged route, end to end through host buffers ----
+    # ---- staged route, end to end through host buffers, every workload ----
     e2e = e2e_compact = e2e_tiled = None
+    bus = None
+    staged = {}
     if not args.no_e2e:
-        e2e = run_e2e(args, w, t, dev, D, B)
-        # whole job: every rank's bytes over the slowest rank's wall time
-        secs = max_over_ranks(e2e.pop("_secs"), world)
-        e2e["value"] = round(whole_job_gbs(kv_bytes, e2e["steps"], secs * 1e3, world), 2)
-        e2e["ms_per_step"] = round(1e3 * secs / e2e["steps"], 3)
-        if not w.window:
-            e2e_tiled = run_e2e(args, w, t, dev, D, B, tiled=True)
-            secs = max_over_ranks(e2e_tiled.pop("_secs"), world)
-            e2e_tiled["value"] = round(whole_job_gbs(kv_bytes, e2e_tiled["steps"], secs * 1e3,
-                                                     world), 2)
-            e2e_tiled["ms_per_step"] = round(1e3 * secs / e2e_tiled["steps"], 3)
-        if not args.no_compact:
-            e2e_compact = run_e2e(args, w, t, dev, D, B, compact=True,
-                                  exact=(res.o.out, res.o.lse))
-            secs = max_over_ranks(e2e_compact.pop("_secs"), world)
-            e2e_compact["value"] = round(whole_job_gbs(kv_bytes, e2e_compact["steps"],
-                                                       secs * 1e3, world), 2)
-            e2e_compact["ms_per_step"] = round(1e3 * secs / e2e_compact["steps"], 3)
+        for name in names:
+            wn, tn = wls[name], ts[name]
+            host = D.HostHistory(wn, tn)
+            kvb = wn.kv_bytes_per_step()
+            staged[name] = finish_e2e(run_e2e(args, wn, tn, dev, D, B, host), kvb, world)
+            if name == args.workload:
+                if not wn.window:
+                    e2e_tiled = finish_e2e(run_e2e(args, wn, tn, dev, D, B, host, tiled=True),
+                                           kvb, world)
+                if not args.no_compact:
+                    e2e_compact = finish_e2e(
+                        run_e2e(args, wn, tn, dev, D, B, host, compact=True,
+                                exact=(summaries_exact(D, wn, tn, dev))), kvb, world)
+            if (name == "1x262144" and not args.no_bus_model_leg and rank == 0
+                    and world == 1):
+                bus = bus_model_from_prefixes(args, wn, tn, host, dev, D)
+            host.close()
+            del host
+            torch.cuda.empty_cache()
+        e2e = staged[args.workload]
+        if bus is not None:
+            legs_pred = {n: staged[n] for n in names}
+            if e2e_tiled is not None:
+                legs_pred[args.workload + " per tile"] = e2e_tiled
+            if e2e_compact is not None:
+                legs_pred[args.workload + " compact"] = e2e_compact
+            bus["legs"] = bus_predictions(bus["_model"], legs_pred)
+            del bus["_model"]
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -476,46 +600,31 @@ def run_ours(args):
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": max(3, args.warmup),
-            "ms_per_step": round(step_ms, 4), "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": head["ms_per_step"], "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "batch": w.batch,
-                       "ctx": int(w.lengths[0]) if w.batch == 1 or len(set(w.lengths)) == 1
-                       else [int(x) for x in w.lengths],
-                       "layers": w.n_layers, "heads": "24q/4kv", "head_dim": 256,
-                       "page_tokens": 64, "tiles_per_request": w.n_tiles,
-                       "route": "resident", "parallelism": f"replicas x{world}",
-                       "l2": (f"inputs larger than L2 ({kv_bytes / 1e9:.2f} GB of KV per step)"
-                              if kv_bytes > 2 * L2_BYTES else
-                              f"no flush; {kv_bytes / 1e6:.0f} MB of KV per step is within "
-                              "twice the 129 MB L2, so part of it may hit there"),
-                       "kernel": "cuda-core fp32" if args.cuda_core
-                       else "tensor-core mma.sync bf16 + TMA pipeline"
-                       + (", tail write and tile merge fused" if fused else "")
-                       + (", early page loads" if kv_ready else ""),
-                       "accumulate": "fp32"},
-            "tokens_per_s": round(tokens_per_s, 1),
-            "pct_of_hbm_peak": round(100 * value / peak, 2),
-            "gpu_launches": launches_per_step * args.steps,
-            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                         "peak_kind": peak_kind, "unit": "GB/s",
-                         "frac": round(achieved / peak, 4),
-                         "frac_of_nominal_8000": round(achieved / 8000.0, 4),
-                         "traffic": recorded_traffic() if args.workload == "4x31744" else None,
-                         "kernel": "paged_decode_kernel",
-                         "bytes_per_launch": kv_bytes_layer,
-                         "mean_launch_ms": round(kern_ms, 5),
-                         "launch_ms_from": kern_how,
-                         "eager_launch_ms": round(eager_ms, 5)},
+            "config": workload_config(w, world, fused, kv_ready, args),
+            "tokens_per_s": head["tokens_per_s"],
+            "pct_of_hbm_peak": head["pct_of_hbm_peak"],
+            "gpu_launches": (1 if fused else 2 + int(w.n_tiles > 1)) * w.n_layers * args.steps,
+            "gpu_launches_all_resident_regions": leg_launches(names, wls, args) * args.steps,
+            "roofline": head["roofline"],
             "clocks": clk,
-            "host_issue_ms_per_step": round(1e3 * host_issue_s / args.steps, 4),
+            "host_issue_ms_per_step": head["host_issue_ms_per_step"],
             "null_arm": {"ms_per_step": round(null_ms, 4),
                          "what": "the same launches with one-token tiles (the new token "
                                  "only): the step's fixed cost, outside the timed region"},
-            "step_launch": f"CUDA graph of the {launches_per_step} launches of one step, "
-                           "replayed per step",
+            "step_launch": "CUDA graph of one step's launches, replayed per step",
         }
+        if len(names) > 1:
+            line["workloads"] = {}
+            for n in names:
+                entry = dict(summaries[n])
+                entry["config"] = workload_config(wls[n], world, fused, kv_ready, args)
+                if n in staged:
+                    entry["e2e"] = staged[n]
+                line["workloads"][n] = entry
         if merge_stress is not None:
             line["merge_stress"] = merge_stress
         if e2e is not None:
@@ -526,12 +635,31 @@ def run_ours(args):
             line["e2e_compact"] = e2e_compact
         if e2e_tiled is not None:
             line["e2e_tiled"] = e2e_tiled
+        if bus is not None:
+            line["bus_model"] = bus
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def leg_launches(names, wls, args):
+    """Our kernel launches per step over every workload's resident timed
+    region (the value reported as gpu_launches is this times the steps)."""
+    fused = not (args.cuda_core or args.unfused)
+    return sum((1 if fused else 2 + int(wls[n].n_tiles > 1)) * wls[n].n_layers for n in names)
+
+
+def summaries_exact(D, w, t, dev):
+    """Merged outputs of the exact resident route (one step), to report how
+    far the compact route moves them."""
+    import torch
+    res = D.ResidentDecode(w, t, stream=torch.cuda.current_stream(dev))
+    res.step()
+    torch.cuda.synchronize(dev)
+    return res.o.out.clone(), res.o.lse.clone()
 
 
 def null_arm(args, w, t, D, B, dev, fused, kv_ready):
@@ -661,16 +789,88 @@ def run_e2e_resident(args, w, t, o, graph, dev):
                      "host memory, the step's graph, merged outputs and LSEs out"}
 
 
-def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
+def timeline_stats(events, n_slots, stage_bytes, steps):
+    """Where the H2D stream's time went in a staged leg's timed region, from
+    the five events of every stage (decode._stage_marks): each stage's copy
+    time (from when its stream reached it and its slot's previous attention
+    and write-back were done, to its copies' end), the H2D stream's idle time
+    before a stage because the host had not issued it yet (host gap) or
+    because the slot's previous readers were still running (slot wait), and
+    the compute stream's idle time between attentions."""
+    if not events:
+        return None
+    ref = events[0][0]
+    tt = [[ref.elapsed_time(e) for e in ev] for ev in events]
+    n = len(tt)
+    per_step = len(stage_bytes)
+    copy_ms, gbps, host_gap, slot_wait, comp_wait, attn = [], [], [], [], [], []
+    for j, (s0, s1, c2, c3, d4) in enumerate(tt):
+        wait_end = -float("inf")
+        if j >= n_slots:
+            pj = tt[j - n_slots]
+            wait_end = max(pj[3], pj[4])
+        start = max(s0, wait_end)
+        c = s1 - start
+        copy_ms.append(c)
+        nb = stage_bytes[j % per_step]
+        if nb > 0 and c > 0:
+            gbps.append(nb / (c / 1e3) / 1e9)
+        slot_wait.append(max(0.0, wait_end - s0))
+        if j >= 1:
+            host_gap.append(max(0.0, s0 - tt[j - 1][1]))
+            comp_wait.append(max(0.0, c2 - tt[j - 1][3]))
+        attn.append(c3 - c2)
+    region = tt[-1][1] - tt[0][0]
+    split = {"copying": sum(copy_ms), "slot_wait": sum(slot_wait), "host_gap": sum(host_gap)}
+    return {
+        "stages": n,
+        "copy_ms": {"median": round(statistics.median(copy_ms), 4),
+                    "min": round(min(copy_ms), 4), "max": round(max(copy_ms), 4)},
+        "copy_GBps": ({"median": round(statistics.median(gbps), 2), "min": round(min(gbps), 2),
+                       "max": round(max(gbps), 2)} if gbps else None),
+        "h2d_region_ms": round(region, 3),
+        "h2d_time_split": {k: round(v / region, 4) for k, v in split.items()} if region > 0
+        else None,
+        "host_gap_ms_per_step": round(sum(host_gap) / steps, 4),
+        "slot_wait_ms_per_step": round(sum(slot_wait) / steps, 4),
+        "compute_wait_ms_per_step": round(sum(comp_wait) / steps, 4),
+        "attention_ms_median": round(statistics.median(attn), 4),
+    }
+
+
+def timeline_reading(tl):
+    """One sentence naming what bounded the H2D stream in the timed region."""
+    split = tl.get("h2d_time_split") or {}
+    cg = tl.get("copy_GBps") or {}
+    copying = split.get("copying", 0.0)
+    if copying >= 0.98:
+        return (f"link-bound: the H2D stream was copying {100 * copying:.1f}% of the timed "
+                f"region (host gaps {100 * split.get('host_gap', 0):.2f}%, slot waits "
+                f"{100 * split.get('slot_wait', 0):.2f}%); stage copies ran at "
+                f"{cg.get('median')} GB/s median, {cg.get('min')} GB/s in the slowest stage")
+    worst = max(("host_gap", "slot_wait"), key=lambda k: split.get(k, 0.0))
+    what = {"host_gap": "waiting for the host to issue the next stage",
+            "slot_wait": "waiting for a slot's previous attention and write-back"}[worst]
+    return (f"the H2D stream was copying {100 * copying:.1f}% of the timed region and "
+            f"{what} {100 * split.get(worst, 0):.1f}%")
+
+
+def run_e2e(args, w, t, dev, D, B, host, compact=False, exact=None, tiled=False):
     """Staged route: host-owned history, host Q / new rows in, outputs out.
 
     compact=True: every page below the new token is first converted by the
     background compactor and staged in its compact form once published
     ("runs of two representations"); ``exact`` = (out, lse) of the exact
-    route, to report how far the compact form moves the result."""
+    route, to report how far the compact form moves the result.
+
+    Three measurements: ``steps`` (at most 10) steps back to back, timed on
+    the host (the value), with the stage events recorded (the timeline);
+    one-stream copies of the same host memory before and after (the link
+    probes); and route/probe pairs: a single step, drained, then one copy of
+    every layer's history on one stream, alternated ``--ab-pairs`` times, so
+    the route and the link it is compared with see the same neighbours."""
     import torch
     geo = w.geometry
-    host = D.HostHistory(w, t)
     compute = torch.cuda.current_stream(dev)
     store = None
     convert_s = 0.0
@@ -734,28 +934,50 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
     probe_before = link_probe()
     probe_all_before = link_probe_all()
     steps = max(3, min(args.steps, 10))
+    st.timeline = []
+    issue_s = 0.0
     t0 = time.perf_counter()
     for _ in range(steps):
+        h0 = time.perf_counter()
         step()
+        issue_s += time.perf_counter() - h0
     st.drain()
     torch.cuda.synchronize(dev)
     secs = time.perf_counter() - t0
+    events, st.timeline = st.timeline, None
     if st.kernel_status() != 0:
         raise RuntimeError("staged route kernel status non-zero")
     stats = st.handle.stats()
     staged_per_step = stats.staged_bytes // stats.stage_generation * st.stages_per_step()
     probe_after = link_probe()
     probe_all_after = link_probe_all()
+    # route/probe pairs
+    pairs = []
+    for _ in range(max(0, args.ab_pairs)):
+        torch.cuda.synchronize(dev)
+        a0 = time.perf_counter()
+        step()
+        st.drain()
+        torch.cuda.synchronize(dev)
+        dt = time.perf_counter() - a0
+        pairs.append((dt, link_probe_all()))
+    if st.kernel_status() != 0:
+        raise RuntimeError("staged route kernel status non-zero after the pairs")
     del dst
     h2d = q_host.numel() * 2 + rows_host.numel() * 2 + staged_per_step
     d2h = out_host.numel() * 4 + lse_host.numel() * 4 + w.n_layers * w.batch * geo.row_bytes
     kv = w.kv_bytes_per_step()
+    tl = timeline_stats(events, 2, st.stage_bytes(), steps)
+    if tl is not None:
+        tl["host_issue_ms_per_step"] = round(1e3 * issue_s / steps, 4)
+        tl["reading"] = timeline_reading(tl)
     res = {"value": round(kv * steps / secs / 1e9, 2), "unit": UNIT,
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
            "route": ("host-staged per tile, 2 tile slots" if tiled
                      else "host-staged, 2 arena slots") + ", tail write-back"
                     + (", published pages staged compact" if compact else ""),
            "arena_bytes": int(st.arena_bytes()),
+           "staged_bytes_per_step": int(staged_per_step),
            "ms_per_step": round(1e3 * secs / steps, 3),
            "h2d_GBps": round(staged_per_step * steps / secs / 1e9, 2),
            "link_probe_h2d_GBps": [round(probe_before, 2), round(probe_after, 2)],
@@ -763,7 +985,23 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
                                                round(probe_all_after, 2)],
            "link_probe": "one stream, before and after the timed steps: the first layer's "
                          "history three times, and every layer's history once",
+           "timeline": tl,
            "steps": steps, "_secs": secs}
+    if pairs:
+        step_s = [p[0] for p in pairs]
+        ratios = [(staged_per_step / p[0]) / (p[1] * 1e9) for p in pairs]
+        res["pairs"] = {
+            "n": len(pairs),
+            "step_ms_median": round(1e3 * statistics.median(step_s), 3),
+            "step_ms": [round(1e3 * x, 3) for x in step_s],
+            "route_h2d_GBps_median": round(staged_per_step / statistics.median(step_s) / 1e9, 2),
+            "probe_all_layers_GBps": [round(p[1], 2) for p in pairs],
+            "route_over_probe_median": round(statistics.median(ratios), 4),
+            "route_over_probe_min": round(min(ratios), 4),
+            "what": "a single step (drained) then one copy of every layer's history on one "
+                    "stream, alternated; the ratio is the step's staged bytes over its time "
+                    "against the probe right after it",
+        }
     if compact:
         exact_bytes = sum(run.get("n_rows", 0) * geo.row_bytes
                           for reqs in st.exact_plan for _, _, runs in reqs for run in runs
@@ -789,87 +1027,126 @@ def run_e2e(args, w, t, dev, D, B, compact=False, exact=None, tiled=False):
     st.close()
     if store is not None:
         store.close()
-    host.close()
     return res
 
 
-def run_bus_model(args):
-    """Staged-route step time at 32K, 64K, 128K and 262K tokens (1 request,
-    all layers), fitted as t = fixed + bytes / bandwidth."""
+BUS_CONTEXTS = (32768, 65536, 131072, 262144)
+
+
+def bus_points(args, w, t, host, dev, D, contexts=BUS_CONTEXTS, rounds=9):
+    """Single-step times of the staged route (2 arena slots, every layer,
+    drained after each step) for one request at each context length: the
+    first L tokens of a one-request workload's history, staged from its own
+    pinned host segments (the steps' tail write-backs overwrite row L - 1 of
+    those segments).  The contexts are measured in interleaved rounds (one
+    step of each per round), so a burst of load on the shared host link hits
+    every context alike instead of one point; each point is the median over
+    the rounds."""
     import torch
-    from paged_decode_attention_attn_gb300 import busmodel as bm
-    from paged_decode_attention_attn_gb300 import decode as D
     from paged_decode_attention_attn_gb300 import workloads as wl
-    dev = torch.device("cuda", 0)
-    def measure(L, compact):
-        w = wl.custom([L], [[(0, L)]], seed=31, n_layers=args.layers, n_spare=2)
-        t = wl.materialize(w, dev)
-        host = D.HostHistory(w, t)
-        store = None
-        if compact:
-            store = D.CompactStore(w, host, n_threads=max(1, min(16, cpu_cores())))
-            store.mark_written(w.lengths)
-            store.compactor.wait_idle()
-        st = D.StagedDecode(w, t, host, n_slots=2, compact=store)
+    routes = []
+    for L in contexts:
+        if L > int(w.lengths[0]):
+            continue
+        n_pages = -(-L // w.geometry.page_tokens)
+        wp = wl.DecodeWorkload(f"prefix-{L}", w.seed, w.n_layers, np_array([L]),
+                               np_tiles(L), w.page_table[:, :max(1, n_pages)].copy(),
+                               w.pool_pages, w.spare_pages, w.geometry)
+        tp = dict(t)
+        tp["positions"] = torch.full((1,), L - 1, dtype=torch.int32, device=dev)
+        st = D.StagedDecode(wp, tp, host, n_slots=2)
         for _ in range(2):
             st.step()
         st.drain()
-        torch.cuda.synchronize(dev)
-        # fastest of single-step times: the host side is shared, and a
-        # neighbour's burst on the link (seen to stretch single steps by
-        # 40-90%) must not bend the fit; the median is reported beside it
-        times = []
-        for _ in range(7):
+        routes.append((L, wp, st, []))
+    torch.cuda.synchronize(dev)
+    for _ in range(rounds):
+        for L, wp, st, times in routes:
             t0 = time.perf_counter()
             st.step()
             st.drain()
             torch.cuda.synchronize(dev)
             times.append(time.perf_counter() - t0)
-        secs = min(times)
-        med_secs[(L, compact)] = statistics.median(times)
+    pts = []
+    for L, wp, st, times in routes:
+        if st.kernel_status() != 0:
+            raise RuntimeError("bus-model step kernel status non-zero")
         stats = st.handle.stats()
-        staged = stats.staged_bytes // stats.stage_generation * w.n_layers
+        staged = stats.staged_bytes // stats.stage_generation * wp.n_layers
         st.close()
-        if store is not None:
-            store.close()
-        host.close()
-        del st, host, t
-        torch.cuda.empty_cache()
-        return staged, secs
+        pts.append({"ctx": L, "staged_bytes": int(staged),
+                    "median_s": statistics.median(times), "min_s": min(times),
+                    "max_s": max(times)})
+    return pts
 
-    points, rows = [], []
-    med_secs = {}
-    contexts = (32768, 65536, 131072, 262144)
-    for L in contexts:
-        staged, secs = measure(L, False)
-        points.append((staged, secs))
-        rows.append({"ctx": L, "staged_bytes": int(staged), "step_ms": round(1e3 * secs, 3),
-                     "median_step_ms": round(1e3 * med_secs[(L, False)], 3)})
-    model = bm.fit(points)
-    ends = bm.fit([points[0], points[-1]])
-    for r, e in zip(rows, bm.relative_errors(model, points)):
-        r["fit_error_pct"] = round(100 * e, 3)
-    # the compact route predicted from its bytes alone by the model fitted above
-    compact_rows = []
-    if not args.no_compact:
-        for L in contexts:
-            staged, secs = measure(L, True)
-            pred = model.predict(staged)
-            compact_rows.append({"ctx": L, "staged_bytes": int(staged),
-                                 "step_ms": round(1e3 * secs, 3),
-                                 "median_step_ms": round(1e3 * med_secs[(L, True)], 3),
-                                 "predicted_ms": round(1e3 * pred, 3),
-                                 "error_pct": round(100 * (pred - secs) / secs, 3)})
-    print(json.dumps({
-        "bus_model": {k: round(v, 4) for k, v in model.as_dict().items()},
-        "worst_error_pct": round(100 * bm.worst_relative_error(model, points), 3),
-        "endpoint_model": {k: round(v, 4) for k, v in ends.as_dict().items()},
-        "endpoint_model_worst_error_pct":
-            round(100 * bm.worst_relative_error(ends, points), 3),
-        "points": rows, "layers": args.layers, "route": "host-staged, 2 arena slots",
-        "timing": "fastest of 7 single steps per point (median beside it)",
-        "compact_points": compact_rows}),
-        flush=True)
+
+def np_array(x):
+    import numpy as np
+    return np.asarray(x, dtype=np.int64)
+
+
+def np_tiles(L):
+    import numpy as np
+    return np.array([[[0, L]]], dtype=np.int32)
+
+
+def bus_model_from_prefixes(args, w, t, host, dev, D):
+    """Fit t = fixed + bytes / bandwidth on the median single steps at 32K to
+    262K tokens ("KV-cache engineering", section "Costing the bus before
+    changing anything": the model is judged by its worst error over that
+    range)."""
+    from paged_decode_attention_attn_gb300 import busmodel as bm
+    pts = bus_points(args, w, t, host, dev, D)
+    xy = [(p["staged_bytes"], p["median_s"]) for p in pts]
+    model = bm.fit(xy)
+    errs = bm.relative_errors(model, xy)
+    return {
+        "_model": model,
+        "fit": {k: round(v, 4) for k, v in model.as_dict().items()},
+        "fitted_on": "median per context of 9 interleaved rounds of single staged steps "
+                     "(2 arena slots, drained), 1 request, every layer",
+        "worst_error_pct": round(100 * max(errs), 3),
+        "points": [{"ctx": p["ctx"], "staged_bytes": p["staged_bytes"],
+                    "median_ms": round(1e3 * p["median_s"], 3),
+                    "min_ms": round(1e3 * p["min_s"], 3), "max_ms": round(1e3 * p["max_s"], 3),
+                    "predicted_ms": round(1e3 * model.predict(p["staged_bytes"]), 3),
+                    "error_pct": round(100 * e, 3)} for p, e in zip(pts, errs)],
+    }
+
+
+def bus_predictions(model, legs):
+    """The fitted model's prediction of each staged leg's median single step
+    (its route/probe pairs) from the bytes it stages."""
+    out = {}
+    for name, e in legs.items():
+        pr = e.get("pairs")
+        if not pr:
+            continue
+        meas = pr["step_ms_median"]
+        pred = 1e3 * model.predict(e["staged_bytes_per_step"])
+        out[name] = {"staged_bytes": e["staged_bytes_per_step"], "measured_ms": meas,
+                     "predicted_ms": round(pred, 3),
+                     "error_pct": round(100 * (pred - meas) / meas, 3)}
+    if out:
+        worst = max(abs(v["error_pct"]) for v in out.values())
+        out = {"per_leg": out, "worst_abs_error_pct": round(worst, 3)}
+    return out
+
+
+def run_bus_model(args):
+    """The bus model alone: staged steps of 1 request at 32K-262K tokens."""
+    import torch
+    from paged_decode_attention_attn_gb300 import decode as D
+    from paged_decode_attention_attn_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    w = wl.one_request_262144(n_layers=args.layers)
+    t = wl.materialize(w, dev)
+    host = D.HostHistory(w, t)
+    res = bus_model_from_prefixes(args, w, t, host, dev, D)
+    del res["_model"]
+    host.close()
+    res["layers"] = args.layers
+    print(json.dumps({"bus_model": res}), flush=True)
 
 
 def main():

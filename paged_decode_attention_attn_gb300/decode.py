@@ -77,6 +77,39 @@ class _Outputs:
                                          dtype=torch.int32, device=device)
 
 
+def _stage_marks(timeline, h2d):
+    """Timing events of one stage, when ``timeline`` is a list (measurement
+    only; the routes run without them).  Five events per stage:
+      0  on the H2D stream before the stage's waits and copies are enqueued
+      1  on the H2D stream after its copies and page-table fill
+      2  on the compute stream after its wait on the copy event
+      3  on the compute stream after the attention kernels
+      4  on the D2H stream after the tail write-back (or the stage's end)
+    """
+    if timeline is None:
+        return None
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev[0].record(h2d)
+    return ev
+
+
+def _stage_marks_mid(ev, h2d, compute):
+    if ev is not None:
+        ev[1].record(h2d)
+        ev[2].record(compute)
+
+
+def _stage_marks_end(timeline, ev, compute):
+    if ev is not None:
+        ev[3].record(compute)
+        timeline.append(ev)
+
+
+def _stage_marks_wb(ev, d2h):
+    if ev is not None:
+        ev[4].record(d2h)
+
+
 class ResidentDecode:
     """Decode step over a device-resident pool [layers][pages][64][row_elems]."""
 
@@ -151,7 +184,8 @@ class HostHistory:
         for i in range(len(self.layers)):
             for r, L in enumerate(lengths):
                 off = self.offsets[(i, r)]
-                self.rows[off:off + L].copy_(history_rows(w, t["pool"][i], r).cpu())
+                # device rows straight into the pinned segment
+                self.rows[off:off + L].copy_(history_rows(w, t["pool"][i], r))
         # the new token's host row is unknown until the write-back
         for i in range(len(self.layers)):
             for r, L in enumerate(lengths):
@@ -250,6 +284,7 @@ class StagedDecode:
         self.compact = compact
         self.leases = leases
         self.fused = fused
+        self.timeline = None       # a list: timing events of every stage (see stage_marks)
         self.step_index = 0
         self.receipts = []
         self.n_layers = t["pool"].shape[0]
@@ -373,18 +408,24 @@ class StagedDecode:
     def stages_per_step(self) -> int:
         return self.n_layers
 
-    def staged_bytes_per_step(self) -> int:
-        """Host-to-device bytes the current plan moves per step."""
+    def stage_bytes(self) -> list:
+        """Host-to-device bytes of each stage of a step (one per layer)."""
         geo = self.w.geometry
-        total = 0
+        out = []
         for reqs in self.plan:
+            total = 0
             for _, _, runs in reqs:
                 for run in runs:
                     if "host_compact" in run:
                         total += run["n_pages"] * self.compact.page_bytes
                     elif "host_rows" in run:
                         total += run["n_rows"] * geo.row_bytes
-        return total
+            out.append(total)
+        return out
+
+    def staged_bytes_per_step(self) -> int:
+        """Host-to-device bytes the current plan moves per step."""
+        return sum(self.stage_bytes())
 
     def _kernels(self, i: int, table):
         t, o, geo = self.t, self.o, self.w.geometry
@@ -409,10 +450,14 @@ class StagedDecode:
         self.step_index += 1
 
     def layer(self, i: int):
+        tl = _stage_marks(self.timeline, self.h2d)
         slot, _ = self.handle.stage_layer(i, self.plan[i])
+        _stage_marks_mid(tl, self.h2d, self.compute)
         self._kernels(i, self.page_tables[slot])
+        _stage_marks_end(self.timeline, tl, self.compute)
         self.handle.mark_attention_done(i)
         self.handle.writeback_tail(i, self.tails[i])
+        _stage_marks_wb(tl, self.d2h)
 
     def step(self):
         if self.leases:
@@ -483,6 +528,7 @@ class TiledStagedDecode:
         self.h2d = torch.cuda.Stream(dev)
         self.d2h = torch.cuda.Stream(dev)
         self.units = tile_units(w)
+        self.timeline = None       # a list: timing events of every stage (see stage_marks)
         self.slot_pages = max([-(-e // pt) - s // pt for _, _, s, e in self.units if e > s],
                               default=1)
         self.arena = torch.full((n_slots * self.slot_pages, pt, geo.row_elems), float("nan"),
@@ -504,6 +550,20 @@ class TiledStagedDecode:
     def stages_per_step(self) -> int:
         return self.n_layers * sum(1 for _, _, s, e in self.units if e > s)
 
+    def stage_bytes(self) -> list:
+        """Host-to-device bytes of each stage of a step: one per non-empty
+        (layer, request, tile), in issue order."""
+        w, pt, rb = self.w, self.w.geometry.page_tokens, self.w.geometry.row_bytes
+        out = []
+        for _ in range(self.n_layers):
+            for r, _, s, e in self.units:
+                if e <= s:
+                    continue
+                L = int(w.lengths[r])
+                p0, p1 = s // pt, -(-e // pt)
+                out.append(max(0, min(p1 * pt, L - 1) - p0 * pt) * rb)
+        return out
+
     def layer(self, i: int):
         w, geo = self.w, self.w.geometry
         pt = geo.page_tokens
@@ -517,15 +577,19 @@ class TiledStagedDecode:
             rows = min(p1 * pt, L - 1) - p0 * pt
             owner = (i << 32) | r
             key = i * len(self.units) + u
+            tl = _stage_marks(self.timeline, self.h2d)
             slot, _ = self.handle.stage_layer(key, [(r, owner, [dict(
                 logical_page=p0, n_pages=p1 - p0, n_rows=max(0, rows),
                 host_rows=self.host.row_address(i, r, p0 * pt))])])
+            _stage_marks_mid(tl, self.h2d, self.compute)
             tile_kernels(w, self.t, i, r, k, s, e, self.arena,
                          self.page_tables[slot][r:r + 1], self.o, self.workspace, self.compute)
+            _stage_marks_end(self.timeline, tl, self.compute)
             self.handle.mark_attention_done(key)
             if s <= L - 1 < e:
                 self.handle.writeback_tail(key, [(r, L - 1, self.host.row_address(i, r, L - 1),
                                                   owner)])
+            _stage_marks_wb(tl, self.d2h)
         if w.n_tiles > 1:
             o = self.o
             B.lse_merge(o.tile_out[i].view(-1, geo.n_q_heads, geo.head_dim),

@@ -36,6 +36,17 @@ def test_bench_line_has_the_contract_keys():
     for k in ("value", "unit", "h2d_bytes_per_step", "d2h_bytes_per_step"):
         assert k in e, k
     assert e["h2d_bytes_per_step"] > 0 and e["d2h_bytes_per_step"] > 0
+    assert e["timeline"]["stages"] > 0 and e["timeline"]["reading"]
+    assert e["pairs"]["n"] >= 1 and e["pairs"]["route_over_probe_median"] > 0
+    # the metric's other workloads, each with its resident value, roofline and staged e2e
+    wk = d["workloads"]
+    assert set(wk) == {"4x31744", "1x262144", "ragged", "1x32768"}
+    for name, entry in wk.items():
+        assert entry["value"] > 0 and 0 < entry["roofline"]["frac"] < 2, name
+        assert entry["e2e"]["value"] > 0 and entry["e2e"]["timeline"]["stages"] > 0, name
+    bm = d["bus_model"]
+    assert len(bm["points"]) == 4 and bm["fit"]["link_GBps"] > 0
+    assert "worst_error_pct" in bm and bm["legs"]["per_leg"]
     c = d["cpu_baseline"]
     assert c["kind"] == "oracle" and c["cores"] == 2 and c["value"] > 0 and c["sample"]
     for k in ("sm_mhz", "sm_max_mhz", "reasons"):
