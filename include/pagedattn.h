@@ -138,14 +138,21 @@ size_t paged_decode_attn_lse_workspace_bytes(int B, int T, int n_q_heads,
  *              [B][T][n_q_heads].
  *   workspace  device buffer of at least the bytes the query above returns,
  *              256-byte aligned, ZERO-FILLED before its first use; every call
- *              leaves it ready for the next (counters return to zero).  Byte 0
- *              holds the int32 status word (PA_STATUS_* bits, sticky until the
- *              caller clears it).  Calls that share a workspace must be ordered
- *              on one stream.
+ *              leaves it ready for the next (counters return to their start
+ *              state).  Byte 0 holds the int32 status word (PA_STATUS_* bits,
+ *              sticky until the caller clears it); byte 4 an int32 diagnostic
+ *              count of CTAs that stopped waiting for the other CTAs of a
+ *              split unit (their share of its merge went to the unit's last
+ *              CTA: same results, a slower launch; normally 0).  Calls that
+ *              share a workspace must be ordered on one stream.
  * Supported: head_dim 256, n_q_heads / n_kv_heads in 1..8, n_kv_heads >= 1.
  * Results depend only on the logical tiles and the device's SM count, not on
- * physical page placement: two calls that differ only in where the pages sit
- * return bit-identical outputs.  Tensor-core (mma.sync bf16) variant. */
+ * physical page placement or timing: two calls that differ only in where the
+ * pages sit return bit-identical outputs.  The CTAs of one launch wait for
+ * each other only to share a split unit's merge, and a CTA that sees no other
+ * CTA of the unit arrive for 50 us leaves its share to the last one, so
+ * launches never depend on all CTAs being resident at once.
+ * Tensor-core (mma.sync bf16) variant. */
 int paged_decode_attn_lse(const void* q, const void* pool, int64_t pool_pages,
                           const int32_t* page_table, int max_pages,
                           const int32_t* tiles, int B, int T,

@@ -12,9 +12,11 @@
 //    pages are laid end to end and cut into one contiguous page range per CTA
 //    (persistent grid, one CTA per SM), so every SM streams the same number of
 //    pages whatever the mix of lengths.  A unit that spans several CTAs leaves
-//    one partial (max, sum, unnormalised output) per CTA; the last CTA to
-//    finish merges them in CTA order, so the result does not depend on timing
-//    or on where pages sit physically.
+//    one partial (max, sum, unnormalised output) per CTA; once the last of
+//    them has arrived, the unit's CTAs merge the partials in slices of the
+//    output, each slice with a fixed summation order, so the result does not
+//    depend on timing, on which CTA merges which slice, or on where pages sit
+//    physically.
 //  * One producer warp streams pages with TMA: per page the K slice and the V
 //    slice of one kv head (64 rows x 512 B each, row stride 4 KiB) as eight
 //    64x64 boxes with the 128-byte swizzle, into a 3-stage mbarrier ring
@@ -69,13 +71,30 @@ constexpr int kSmemBar = kSmemXML + kXMLBytes;
 constexpr int kSmemMisc = kSmemBar + 2 * kStages * 8;
 constexpr int kSmemUsed = kSmemMisc + 64;
 constexpr int kSmemAlloc = kSmemUsed + 1024;             // slack to align to 1 KiB
-constexpr int kMaxGrid = 1024;
 constexpr int kMaxUnitsLarge = 1024;
 constexpr int kMaxUnitsSmall = 64;
 constexpr int kSegmentCharge = 6;  // pages charged per segment when CTAs' shares are cut (measured: 3-8 best)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;         // 2 s per wait
+// A split unit's merge reads up to kMaxPartsPerLane partials per lane of a
+// 32-lane team, which bounds the CTAs a unit may span and so the grid.
+constexpr int kMaxPartsPerLane = 5;
+constexpr int kMaxGrid = 32 * kMaxPartsPerLane;
+// How long a CTA that has stored its partial waits without seeing another
+// CTA of the unit arrive before it leaves its share of the merge to the
+// unit's last CTA.  The CTAs of a launch finish within ~25 us of each other
+// (per-SM streaming speeds differ by up to ~10% over a long launch), with
+// arrivals every few hundred ns; the limit matters only when some of them
+// cannot be resident at the same time (other work holds SMs), where waiting
+// longer would only delay them.
+constexpr uint64_t kSliceWaitNs = 50000ull;
 constexpr size_t kStatusBytes = 256;
-constexpr size_t kCounterBytes = 4 * kMaxUnitsLarge;
+// A split unit's outputs are merged in at most this many slices, one per
+// waiting CTA: enough to spread the partials' loads, few enough that most of
+// a widely split unit's CTAs leave at once (their SMs then take the next
+// launch's first page loads).
+constexpr int kMaxSlices = 16;
+// Per unit: a 64-bit arrival word (count | leavers << 16 | generation << 32).
+constexpr size_t kCounterBytes = 8 * kMaxUnitsLarge;
 constexpr size_t kPartOBytes = size_t(kMaxG) * kD * 4;   // per partial slot
 constexpr size_t kPartMLBytes = size_t(kMaxG) * 2 * 4;
 constexpr float kLn2Hi = 0.693145751953125f;        // ln 2, high bits (exact products)
@@ -88,6 +107,7 @@ constexpr float kLog2e = 1.44269504088896341f;
 constexpr float kRefStep = 8.0f;
 
 static_assert(kSmemAlloc <= 232448, "shared memory budget");
+static_assert(kMaxSlices <= kMaxGrid - 1, "slices per split unit");
 
 struct Unit {
   int32_t bt_g;        // (b * T + t) * Hkv + g
@@ -96,6 +116,7 @@ struct Unit {
   int32_t page_first;  // flattened index of the unit's first page in this launch
   int32_t part_base;   // first partial slot (units covered by several CTAs)
   int32_t n_parts;     // CTAs covering the unit
+  int32_t pair_total;  // completions the (request, kv head) tile counter reaches (fused merge)
 };
 
 template <int kMaxUnits>
@@ -105,7 +126,7 @@ struct Params {
   float* out;
   float* lse;
   int32_t* status;
-  int32_t* counters;
+  unsigned long long* arrivals;  // [unit] split units: CTAs arrived, leavers, generation
   int32_t* req_counters;  // [B][Hkv] tiles finished (fused merge)
   float* part_o;   // [slot][kMaxG][kD]
   float* part_ml;  // [slot][kMaxG][2]
@@ -140,6 +161,13 @@ struct Params {
   float* m_lse;
   Unit units[kMaxUnits];
 };
+// Kernel parameters travel in the 32 KiB parameter space.
+static_assert(sizeof(Params<kMaxUnitsLarge>) <= 32764, "kernel parameters too large");
+
+// Slices a unit split over n >= 2 CTAs is merged in.
+__host__ __device__ __forceinline__ int split_slices(int n) {
+  return n - 1 < kMaxSlices ? n - 1 : kMaxSlices;
+}
 
 __host__ __device__ __forceinline__ int unit_pages(int tok_start, int tok_end) {
   return tok_end > tok_start ? (tok_end + kPage - 1) / kPage - tok_start / kPage : 0;
@@ -198,8 +226,8 @@ struct Shared {
   uint32_t empty_bar;
   volatile int* poison;  // [kStages]
   volatile int* abort_flag;
-  volatile int* merge_flag;
   volatile int* fin_flag;
+  volatile int* merge_info;  // split-unit merge: mode, leavers, finisher
 };
 
 __device__ __forceinline__ Shared carve(uint8_t* raw) {
@@ -214,8 +242,8 @@ __device__ __forceinline__ Shared carve(uint8_t* raw) {
   int* misc = reinterpret_cast<int*>(base + kSmemMisc);
   s.poison = misc;
   s.abort_flag = misc + kStages;
-  s.merge_flag = misc + kStages + 1;
   s.fin_flag = misc + kStages + 2;
+  s.merge_info = misc + 8;
   return s;
 }
 
@@ -247,10 +275,10 @@ constexpr int kDimHalves = 2;
 constexpr int kHalfD = kD / kDimHalves;
 
 // Tensor-core accumulators of one warp: o[n][0..1] = head row (lane/4),
-// dims 128*half + 8n + 2(lane%4) + {0,1}, from P_hi; o[n][2..3] = the same
-// head and dims, from P_lo.
+// dims 128*half + 8n + 2(lane%4) + {0,1}; each page adds its P_hi and P_lo
+// products for those dims (mma rows lane/4 and lane/4 + 8).
 struct MmaState {
-  float o[kHalfD / 8][4];
+  float o[kHalfD / 8][2];
   float m;  // reference of this lane's head row (log2 domain, multiple of 8)
   float l;  // this lane's share of the row sum (quad-reduced at the end)
 };
@@ -261,19 +289,22 @@ struct FmaState {
   float l[kMaxG];
 };
 
-// Called by every consumer thread once a unit's tile output (request b,
-// tile t, kv head g) is written.  With the fused merge, the CTA that finishes
-// the last tile of (b, g) merges its T tiles for the G query heads of g with
-// the merge kernel's own row routine (same bits as lse_merge over those
-// partials), then resets the counter for the next call.
+// Called by every consumer thread once it has stored `done` parts of the
+// tile outputs of (request b, kv head g): a whole unsplit (or empty) unit
+// counts 1, a slice of a split unit 1.  With the fused merge, the CTA whose
+// parts complete the pair's count (`total`, over its T tiles) merges the T
+// tiles for the G query heads of g with the merge kernel's own row routine
+// (same bits as lse_merge over those partials), then resets the counter for
+// the next call.
 template <int kMaxUnits, int kConsumers, int kConsumerWarps>
 __device__ __forceinline__ void finish_unit(const Params<kMaxUnits>& p, const Shared& sh, int b,
-                                            int g, int ct, int warp, int lane) {
+                                            int g, int ct, int warp, int lane, int done,
+                                            int total) {
   if (p.m_out == nullptr) return;
-  ptx::named_barrier(1, kConsumers);       // the unit's outputs are all stored
+  ptx::named_barrier(1, kConsumers);       // this CTA's outputs are all stored
   if (ct == 0) {
-    const int prev = ptx::atomic_add_acq_rel_gpu(p.req_counters + b * p.Hkv + g, 1);
-    *sh.fin_flag = (prev == p.T - 1) ? 1 : 0;
+    const int prev = ptx::atomic_add_acq_rel_gpu(p.req_counters + b * p.Hkv + g, done);
+    *sh.fin_flag = (prev + done == total) ? 1 : 0;
   }
   ptx::named_barrier(1, kConsumers);
   if (*sh.fin_flag) {
@@ -286,6 +317,118 @@ __device__ __forceinline__ void finish_unit(const Params<kMaxUnits>& p, const Sh
     if (ct == 0) p.req_counters[b * p.Hkv + g] = 0;
   }
   ptx::named_barrier(1, kConsumers);
+}
+
+// Merges output float4s [o_lo, o_hi) of a split unit (o = row * kD/4 + float4
+// column) from its n partials (slots part_base ..): the unit's tile output and,
+// at column 0, its LSE.  The same merge rule as the tile merge: common
+// reference = max partial reference, weights exactly 2^(m_c - max), output =
+// weighted sum / summed weights.  Each output is taken by a team of t lanes
+// (t a power of two, as large as one pass over the outputs allows); lane j
+// adds partials j, j + t, ... in that order, and the team adds its lanes'
+// sums by a butterfly.  The arithmetic depends only on n and the range, never
+// on which CTA runs it, so slices merged by different CTAs, or twice, give
+// the same bits.  All of a lane's loads are issued before its arithmetic.
+template <int kMaxUnits, int kConsumers>
+__device__ __forceinline__ void merge_split_slice(const Params<kMaxUnits>& p, int part_base, int n,
+                                                  int o_lo, int o_hi, size_t orow0, int ct) {
+  constexpr int kVec = kD / 4;
+  const int len = o_hi - o_lo;
+  int t = 32;
+  while (t > 1 && kConsumers / t < len && (n + t / 2 - 1) / (t / 2) <= kMaxPartsPerLane) t >>= 1;
+  const int n_teams = kConsumers / t;
+  const int j = ct & (t - 1);
+  const int team = ct / t;
+  const float2* pml = reinterpret_cast<const float2*>(p.part_ml) + (size_t)part_base * kMaxG;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o) + (size_t)part_base * kMaxG * kVec;
+  for (int base = o_lo; base < o_hi; base += n_teams) {
+    const int o = base + team;
+    const bool have = o < o_hi;
+    const int row = have ? o / kVec : 0;
+    const int dv = have ? o - row * kVec : 0;
+    float2 ml[kMaxPartsPerLane];
+    float4 v[kMaxPartsPerLane];
+#pragma unroll
+    for (int k = 0; k < kMaxPartsPerLane; ++k) {
+      const int c = j + k * t;
+      if (have && c < n) {
+        ml[k] = __ldcg(pml + (size_t)c * kMaxG + row);
+        v[k] = __ldcg(po + ((size_t)c * kMaxG + row) * kVec + dv);
+      } else {
+        ml[k] = make_float2(-INFINITY, 0.f);
+        v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+    }
+    float big_m = -INFINITY;
+    int nan = 0;
+#pragma unroll
+    for (int k = 0; k < kMaxPartsPerLane; ++k) {
+      big_m = fmaxf(big_m, ml[k].x);
+      nan |= (ml[k].x != ml[k].x);
+    }
+    for (int off = t >> 1; off > 0; off >>= 1) {
+      big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, off));
+      nan |= __shfl_xor_sync(0xffffffffu, nan, off);
+    }
+    float l = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < kMaxPartsPerLane; ++k) {
+      const float a = ref_weight(ml[k].x, big_m);
+      l = fmaf(a, ml[k].y, l);
+      acc.x = fmaf(a, v[k].x, acc.x);
+      acc.y = fmaf(a, v[k].y, acc.y);
+      acc.z = fmaf(a, v[k].z, acc.z);
+      acc.w = fmaf(a, v[k].w, acc.w);
+    }
+    for (int off = t >> 1; off > 0; off >>= 1) {
+      l += __shfl_xor_sync(0xffffffffu, l, off);
+      acc.x += __shfl_xor_sync(0xffffffffu, acc.x, off);
+      acc.y += __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc.z += __shfl_xor_sync(0xffffffffu, acc.z, off);
+      acc.w += __shfl_xor_sync(0xffffffffu, acc.w, off);
+    }
+    if (have && j == 0) {
+      const size_t orow = orow0 + row;
+      const float qnan = __int_as_float(0x7fc00000);
+      reinterpret_cast<float4*>(p.out + orow * kD)[dv] =
+          nan ? make_float4(qnan, qnan, qnan, qnan)
+              : make_float4(acc.x / l, acc.y / l, acc.z / l, acc.w / l);
+      if (dv == 0) p.lse[orow] = nan ? qnan : lse_of(big_m, l);
+    }
+  }
+}
+
+// Thread 0 of a CTA that has arrived at split unit `arrival` in generation
+// `gen`, with this unit's segment as its last: waits until the unit's last CTA
+// opens the next generation (every partial is then stored and visible).  If
+// no other CTA of the unit arrives for kSliceWaitNs while some have not, it
+// records itself as a leaver (the last CTA then merges every slice) and
+// returns false.  A CTA that finds every CTA arrived keeps waiting (the
+// opening follows the last arrival directly), up to wait_limit_ns.
+__device__ __forceinline__ bool wait_unit_complete(unsigned long long* arrival, unsigned gen,
+                                                   int n, uint64_t wait_limit_ns,
+                                                   int32_t* status) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  uint64_t t_seen = t0;
+  int seen = -1;
+  while (true) {
+    const unsigned long long v = ptx::load_acquire_gpu(arrival);
+    if ((unsigned)(v >> 32) != gen) return true;
+    const uint64_t now = ptx::globaltimer_ns();
+    const int count = (int)(v & 0xffffu);
+    if (count != seen) {
+      seen = count;
+      t_seen = now;
+    }
+    if (count < n) {
+      if (now - t_seen > kSliceWaitNs && ptx::atomic_cas_gpu(arrival, v, v + (1ull << 16)) == v)
+        return false;
+    } else if (now - t0 > wait_limit_ns) {
+      atomicOr(status, PA_STATUS_TIMEOUT);
+      return false;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -311,7 +454,6 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       sh.poison[s] = 0;
     }
     *sh.abort_flag = 0;
-    *sh.merge_flag = 0;
     ptx::mbar_init_fence();
   }
   if (warp == kConsumerWarps && lane == 0) ptx::prefetch_tensormap(&tmap);
@@ -345,8 +487,9 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
   }
 
 
-  const long long cta_start = (long long)blockIdx.x * p.total_pages / p.grid;
-  const long long cta_end = (long long)(blockIdx.x + 1) * p.total_pages / p.grid;
+  // Flattened page range of this CTA (a launch holds fewer than 2^31 pages).
+  const int cta_start = static_cast<int>((long long)blockIdx.x * p.total_pages / p.grid);
+  const int cta_end = static_cast<int>((long long)(blockIdx.x + 1) * p.total_pages / p.grid);
 
   // ======================= producer warp =======================
   if (warp == kConsumerWarps) {
@@ -360,9 +503,9 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       const Unit U = p.units[u];
       const int np = unit_pages(U.tok_start, U.tok_end);
       if (np == 0) continue;
-      const long long pf = U.page_first;
-      const int lo = static_cast<int>(max(cta_start, pf) - pf);
-      const int hi = static_cast<int>(min(cta_end, pf + np) - pf);
+      const int pf = U.page_first;
+      const int lo = max(cta_start, pf) - pf;
+      const int hi = min(cta_end, pf + np) - pf;
       if (hi <= lo) continue;   // only the unit's segment charge falls in this range
       const int bt = U.bt_g / Hkv;
       const int g = U.bt_g - bt * Hkv;
@@ -449,7 +592,8 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       p.out[((size_t)bt * p.Hq + g * G + row) * kD + d] = 0.f;
       if (d == 0) p.lse[(size_t)bt * p.Hq + g * G + row] = -INFINITY;
     }
-    finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, bt / p.T, g, ct, warp, lane);
+    finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, bt / p.T, g, ct, warp, lane, 1,
+                                                       U.pair_total);
   }
 
   int it = 0;
@@ -459,9 +603,9 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     const Unit U = p.units[u];
     const int np = unit_pages(U.tok_start, U.tok_end);
     if (np == 0) continue;
-    const long long pf = U.page_first;
-    const int lo = static_cast<int>(max(cta_start, pf) - pf);
-    const int hi = static_cast<int>(min(cta_end, pf + np) - pf);
+    const int pf = U.page_first;
+    const int lo = max(cta_start, pf) - pf;
+    const int hi = min(cta_end, pf + np) - pf;
     if (hi <= lo) continue;
     const int bt = U.bt_g / Hkv;
     const int g = U.bt_g - bt * Hkv;
@@ -471,8 +615,8 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     // The new token of this request, if it falls in this segment's pages:
     // its K slice (chunk `lane`) and V slice (chunk `lane`) of kv head g.
     // The position's load is issued before the Q loads below and the row's
-    // loads are consumed only at the substitution, so neither adds a round
-    // trip to the segment's start.
+    // loads go out with them, so neither adds a round trip to the segment's
+    // start.
     const int pos = p.new_rows != nullptr ? __ldg(p.positions + b) : -1;
     int sub_pos = -1;
     uint4 sub_k = make_uint4(0u, 0u, 0u, 0u), sub_v = make_uint4(0u, 0u, 0u, 0u);
@@ -486,8 +630,6 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       }
     };
 
-    float* xo_g = sh.xo + (tg * kMaxG) * kXRow;   // this token group's exchange rows
-    float* xml_g = sh.xml + (tg * kMaxG) * 2;
 
     if constexpr (kTensorCores) {
       // ---- Q fragments (A operand rows = heads; rows 8..15 stay zero) ----
@@ -506,11 +648,22 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
           qfrag[kk * 32 + lane] = v;
         }
       }
-      load_new_row();
+      // The new token's K and V slices (32 16-byte chunks each) go beside
+      // the Q fragments, loaded with them whether or not the token falls in
+      // this segment (its position arrives with them), so that neither the
+      // segment's start nor the page loop's registers pay for them.
+      uint4* xrow = reinterpret_cast<uint4*>(sh.xo) + kD / 16 * 32 / 2;
+      if (p.new_rows != nullptr && ct < 64) {
+        const uint4* row = reinterpret_cast<const uint4*>(p.new_rows + (size_t)b * p.row_elems);
+        xrow[ct] = __ldg(row + ((ct < 32 ? g : Hkv + g) * kD) / 8 + (ct & 31));
+      }
+      if (pos >= max(U.tok_start, first_page_tok + lo * kPage) &&
+          pos < min(U.tok_end, first_page_tok + hi * kPage))
+        sub_pos = pos;
       ptx::named_barrier(1, kConsumers);
       MmaState st;
 #pragma unroll
-      for (int n = 0; n < kHalfD / 8; ++n) st.o[n][0] = st.o[n][1] = st.o[n][2] = st.o[n][3] = 0.f;
+      for (int n = 0; n < kHalfD / 8; ++n) st.o[n][0] = st.o[n][1] = 0.f;
       st.m = -INFINITY;
       st.l = 0.f;
 
@@ -541,8 +694,8 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
           // The new token's row: both warps of the group write its K slice
           // (same bytes), each its own half of the V slice.
           const int r = sub_pos - page_tok;
-          put_row_chunk(stage, r, lane, sub_k);
-          if ((lane >> 4) == dh) put_row_chunk(stage + kHalfBytes, r, lane, sub_v);
+          put_row_chunk(stage, r, lane, xrow[lane]);
+          if ((lane >> 4) == dh) put_row_chunk(stage + kHalfBytes, r, lane, xrow[32 + lane]);
           ptx::fence_proxy_async_smem();
           __syncwarp();
         }
@@ -608,8 +761,6 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
             for (int n = 0; n < kHalfD / 8; ++n) {
               st.o[n][0] *= alpha;
               st.o[n][1] *= alpha;
-              st.o[n][2] *= alpha;
-              st.o[n][3] *= alpha;
             }
             st.l *= alpha;
             st.m = m_new;
@@ -644,10 +795,12 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
             float t1[4] = {0.f, 0.f, 0.f, 0.f};
             ptx::mma_bf16_16816(t0, pa0, pa1, pa2, pa3, b0, b1);
             ptx::mma_bf16_16816(t1, pa0, pa1, pa2, pa3, b2, b3);
+            // Rows 0..7 (P_hi) and 8..15 (P_lo) of the same head and dims
+            // add up to the page's product with ~16-bit probabilities.
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-              st.o[2 * nd2][k] += t0[k];
-              st.o[2 * nd2 + 1][k] += t1[k];
+            for (int k = 0; k < 2; ++k) {
+              st.o[2 * nd2][k] += t0[k] + t0[k + 2];
+              st.o[2 * nd2 + 1][k] += t1[k] + t1[k + 2];
             }
           }
         }
@@ -659,15 +812,15 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       st.l += __shfl_xor_sync(0xffffffffu, st.l, 1);
       st.l += __shfl_xor_sync(0xffffffffu, st.l, 2);
       if (gr < G) {
-        float* row = xo_g + gr * kXRow + kHalfD * dh;
+        float* row = sh.xo + (tg * kMaxG + gr) * kXRow + kHalfD * dh;
 #pragma unroll
         for (int n = 0; n < kHalfD / 8; ++n) {
           *reinterpret_cast<float2*>(row + 8 * n + 2 * tq) =
-              make_float2(st.o[n][0] + st.o[n][2], st.o[n][1] + st.o[n][3]);
+              make_float2(st.o[n][0], st.o[n][1]);
         }
         if (tq == 0 && dh == 0) {
-          xml_g[gr * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m;
-          xml_g[gr * 2 + 1] = st.l;
+          sh.xml[(tg * kMaxG + gr) * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m;
+          sh.xml[(tg * kMaxG + gr) * 2 + 1] = st.l;
         }
       }
     } else {
@@ -784,14 +937,14 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
 #pragma unroll
       for (int h = 0; h < kMaxG; ++h) {
         if (h < G) {
-          float* row = xo_g + h * kXRow + 8 * lane;
+          float* row = sh.xo + (tg * kMaxG + h) * kXRow + 8 * lane;
           *reinterpret_cast<float4*>(row) =
               make_float4(st.o[h][0], st.o[h][1], st.o[h][2], st.o[h][3]);
           *reinterpret_cast<float4*>(row + 4) =
               make_float4(st.o[h][4], st.o[h][5], st.o[h][6], st.o[h][7]);
           if (lane == 0) {
-            xml_g[h * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m[h];
-            xml_g[h * 2 + 1] = st.l[h];
+            sh.xml[(tg * kMaxG + h) * 2 + 0] = poisoned ? __int_as_float(0x7fc00000) : st.m[h];
+            sh.xml[(tg * kMaxG + h) * 2 + 1] = st.l[h];
           }
         }
       }
@@ -851,142 +1004,60 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
       }
     }
     if (!single) {
-      // The last CTA to finish this unit merges every partial, in CTA order.
-      // The barrier orders every thread's partial before thread 0's
-      // acquire-release count, which publishes them at device scope and, in
-      // the last CTA, makes every other CTA's partial visible; the barrier
-      // after it extends that to the CTA's threads.
+      // Split unit: CTAs k0 .. k1 each stored a partial.  The barrier orders
+      // every thread's partial before thread 0's acquire-release arrival,
+      // which publishes it at device scope.  The last CTA to arrive opens the
+      // arrival word's next generation; CTAs k0 .. k0 + S - 1 (S <= n - 1:
+      // their page ranges end inside this unit, so it is their last segment)
+      // wait for that and each merges one of S slices of the unit's outputs,
+      // so the merge is spread over S SMs instead of loading every partial
+      // into one.  A CTA that gave up waiting leaves its slice to the last
+      // CTA, which then merges every slice (a slice merged twice gets the
+      // same bits).  The other CTAs leave at once.
+      const int n = U.n_parts;
+      const int S = split_slices(n);
+      const int rank = (int)blockIdx.x - cta_of(pf, p.total_pages, p.grid);
+      const bool participant = rank < S;
+      unsigned long long* arrival = p.arrivals + u;
       ptx::named_barrier(1, kConsumers);
       if (ct == 0) {
-        const int prev = ptx::atomic_add_acq_rel_gpu(p.counters + u, 1);
-        *sh.merge_flag = (prev == U.n_parts - 1) ? 1 : 0;
+        const unsigned long long prev = ptx::atomic_add_acq_rel_gpu(arrival, 1ull);
+        const int arrived = (int)(prev & 0xffffu) + 1;
+        int mode = 0;  // 0: no slice here, 1: this CTA's slice, 2: every slice
+        int leavers = 0;
+        if (arrived == n) {
+          leavers = (int)((prev >> 16) & 0xffffu);
+          // Count and leavers back to zero, generation + 1.
+          ptx::red_add_release_gpu(arrival, (1ull << 32) -
+                                                ((unsigned long long)leavers << 16) -
+                                                (unsigned long long)n);
+          mode = leavers ? 2 : (participant ? 1 : 0);
+          if (leavers) atomicAdd(p.status + 1, leavers);   // diagnostic count, not an error
+        } else if (participant) {
+          mode = wait_unit_complete(arrival, (unsigned)(prev >> 32), n, p.wait_limit_ns,
+                                    p.status) ? 1 : 0;
+        }
+        sh.merge_info[0] = mode;
+        sh.merge_info[1] = leavers;
       }
       ptx::named_barrier(1, kConsumers);
-      if (*sh.merge_flag) {
-        // One CTA finishes the unit while the rest of the grid is idle, so
-        // this is latency-bound: every thread issues all of its loads before
-        // it does any arithmetic (one L2 round trip per phase).
-        const int n = U.n_parts;
-        float* wts = sh.xo;                 // [part][kMaxG]
-        float* row_l = sh.xml;              // [kMaxG]
-        float* row_m = sh.xml + kMaxG;      // [kMaxG]
-        float* row_lse = sh.xml + 2 * kMaxG;  // [kMaxG]
-        const float2* pml = reinterpret_cast<const float2*>(p.part_ml) +
-                            (size_t)U.part_base * kMaxG;
-        for (int row = warp; row < G; row += kConsumerWarps) {
-          // Lanes hold the statistics of partials lane and lane + 32 in
-          // registers (one round trip up to 64 partials); beyond that they
-          // are read again for the weights.
-          const float2 none = make_float2(-INFINITY, 0.f);
-          const float2 first = lane < n ? __ldcg(pml + (size_t)lane * kMaxG + row) : none;
-          const float2 second =
-              lane + 32 < n ? __ldcg(pml + (size_t)(lane + 32) * kMaxG + row) : none;
-          float big_m = fmaxf(first.x, second.x);
-          int nan = (first.x != first.x) | (second.x != second.x);
-          for (int c = lane + 64; c < n; c += 32) {
-            const float mc = __ldcg(pml + (size_t)c * kMaxG + row).x;
-            nan |= (mc != mc);
-            big_m = fmaxf(big_m, mc);
-          }
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            big_m = fmaxf(big_m, __shfl_xor_sync(0xffffffffu, big_m, off));
-            nan |= __shfl_xor_sync(0xffffffffu, nan, off);
-          }
-          float l = 0.f;
-          if (lane < n) {
-            const float a = ref_weight(first.x, big_m);
-            wts[lane * kMaxG + row] = a;
-            l = a * first.y;
-          }
-          if (lane + 32 < n) {
-            const float a = ref_weight(second.x, big_m);
-            wts[(lane + 32) * kMaxG + row] = a;
-            l = fmaf(a, second.y, l);
-          }
-          for (int c = lane + 64; c < n; c += 32) {
-            const float2 ml = __ldcg(pml + (size_t)c * kMaxG + row);
-            const float a = ref_weight(ml.x, big_m);
-            wts[c * kMaxG + row] = a;
-            l = fmaf(a, ml.y, l);
-          }
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
-          if (lane == 0) {
-            const float m_out = nan ? __int_as_float(0x7fc00000) : big_m;
-            row_l[row] = l;
-            row_m[row] = m_out;
-            row_lse[row] = nan ? m_out : lse_of(big_m, l);
-          }
+      const int mode = sh.merge_info[0];
+      if (mode != 0) {
+        const int n_out = G * (kD / 4);
+        for (int sl = mode == 2 ? 0 : rank; sl < (mode == 2 ? S : rank + 1); ++sl) {
+          merge_split_slice<kMaxUnits, kConsumers>(
+              p, U.part_base, n, (int)((long long)sl * n_out / S),
+              (int)((long long)(sl + 1) * n_out / S), (size_t)bt * p.Hq + g * G, ct);
         }
-        ptx::named_barrier(1, kConsumers);
-        // Each thread owns up to two float4 outputs and issues the loads of
-        // both (kBatch partials each) before any arithmetic.  (Issuing the
-        // first batch before the statistics above measured 4% slower.)
-        constexpr int kVec = kD / 4;        // float4 per output row
-        constexpr int kBatch = kTensorCores ? 12 : 6;  // register headroom differs
-        constexpr size_t kPartStride = (size_t)kMaxG * kVec;
-        const float4* po =
-            reinterpret_cast<const float4*>(p.part_o) + (size_t)U.part_base * kPartStride;
-        const int n_out = G * kVec;
-        for (int base = 0; base < n_out; base += 2 * kConsumers) {
-          const int i0 = base + ct;
-          const int i1 = base + kConsumers + ct;
-          const bool h0 = i0 < n_out;
-          const bool h1 = i1 < n_out;
-          const int r0 = h0 ? i0 / kVec : 0;
-          const int r1 = h1 ? i1 / kVec : 0;
-          const float4* s0p = po + (size_t)r0 * kVec + (h0 ? i0 - r0 * kVec : 0);
-          const float4* s1p = po + (size_t)r1 * kVec + (h1 ? i1 - r1 * kVec : 0);
-          float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f);
-          float4 a1 = make_float4(0.f, 0.f, 0.f, 0.f);
-          for (int c = 0; c < n; c += kBatch) {
-            // Past the last partial, reload the last one with weight 0.
-            float4 v0[kBatch], v1[kBatch];
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-              const size_t off = (size_t)min(c + k, n - 1) * kPartStride;
-              v0[k] = h0 ? __ldcg(s0p + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-              v1[k] = h1 ? __ldcg(s1p + off) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int k = 0; k < kBatch; ++k) {
-              const int cc = min(c + k, n - 1);
-              const float w0 = (c + k < n) ? wts[cc * kMaxG + r0] : 0.f;
-              const float w1 = (c + k < n) ? wts[cc * kMaxG + r1] : 0.f;
-              a0.x = fmaf(w0, v0[k].x, a0.x);
-              a0.y = fmaf(w0, v0[k].y, a0.y);
-              a0.z = fmaf(w0, v0[k].z, a0.z);
-              a0.w = fmaf(w0, v0[k].w, a0.w);
-              a1.x = fmaf(w1, v1[k].x, a1.x);
-              a1.y = fmaf(w1, v1[k].y, a1.y);
-              a1.z = fmaf(w1, v1[k].z, a1.z);
-              a1.w = fmaf(w1, v1[k].w, a1.w);
-            }
-          }
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            const bool have = half ? h1 : h0;
-            if (!have) continue;
-            const int idx = half ? i1 : i0;
-            const int row = half ? r1 : r0;
-            const int dv = idx - row * kVec;
-            const float4 acc = half ? a1 : a0;
-            const float big_m = row_m[row];
-            const bool nan = big_m != big_m;
-            const float rl = row_l[row];
-            const size_t orow = (size_t)bt * p.Hq + g * G + row;
-            reinterpret_cast<float4*>(p.out + orow * kD)[dv] =
-                nan ? make_float4(big_m, big_m, big_m, big_m)
-                    : make_float4(acc.x / rl, acc.y / rl, acc.z / rl, acc.w / rl);
-            if (dv == 0) p.lse[orow] = row_lse[row];
-          }
-        }
-        if (ct == 0) p.counters[u] = 0;
-        finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, b, g, ct, warp, lane);
+        // Each slice counts once toward the pair's tile count (the slices
+        // of leavers are counted by the last CTA, which merged them).
+        const int done = mode == 2 ? sh.merge_info[1] + (participant ? 1 : 0) : 1;
+        finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, b, g, ct, warp, lane, done,
+                                                           U.pair_total);
       }
     } else {
-      finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, b, g, ct, warp, lane);
+      finish_unit<kMaxUnits, kConsumers, kConsumerWarps>(p, sh, b, g, ct, warp, lane, 1,
+                                                         U.pair_total);
     }
     ptx::named_barrier(1, kConsumers);
   }
@@ -1014,9 +1085,11 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// Partial slots reserved: one per unit of a launch plus one per CTA (a CTA
+// adds at most one split point), with room for grids up to 1,024 CTAs.
 size_t part_slots(int B, int T, int Hkv) {
   const long long units = (long long)B * T * Hkv;
-  return (size_t)std::min<long long>(units, kMaxUnitsLarge) + kMaxGrid;
+  return (size_t)std::min<long long>(units, kMaxUnitsLarge) + 1024;
 }
 
 // Per (request, kv head) counters of finished tiles for the fused merge.
@@ -1178,7 +1251,7 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
   common.lse = lse;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   common.status = reinterpret_cast<int32_t*>(ws);
-  common.counters = reinterpret_cast<int32_t*>(ws + kStatusBytes);
+  common.arrivals = reinterpret_cast<unsigned long long*>(ws + kStatusBytes);
   const size_t slots = part_slots(B, T, n_kv_heads);
   const size_t rc_bytes = request_counter_bytes(B, n_kv_heads);
   common.req_counters = reinterpret_cast<int32_t*>(ws + kStatusBytes + kCounterBytes);
@@ -1206,6 +1279,14 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
 
   // Launches of at most kMaxUnitsLarge units each; every launch partitions its
   // own pages and reuses the workspace after the previous one (same stream).
+  // All launches are laid out first: the fused merge's per-(request, kv
+  // head) count spans every launch that holds a tile of the pair.
+  struct Launch {
+    size_t u0, n;
+    long long total;
+    int grid;
+  };
+  std::vector<Launch> launches;
   for (size_t u0 = 0; u0 < units.size(); u0 += kMaxUnitsLarge) {
     const size_t n = std::min<size_t>(kMaxUnitsLarge, units.size() - u0);
     // The CTAs' equal shares are cut from the units' pages laid end to end,
@@ -1240,19 +1321,33 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
     if ((size_t)part_cursor > slots)
       return fail(PA_ERR_INVALID, "internal: %d partial slots exceed the %zu reserved",
                   part_cursor, slots);
-    const long long eff_total = total > 0 ? total : 1;
-    common.n_requests = u0 == 0 ? B : 0;   // new rows are stored by the first launch
+    launches.push_back({u0, n, total > 0 ? total : 1, grid});
+  }
+  // Completions each (request, kv head) pair's tile count reaches: one per
+  // unsplit or empty unit, one per merge slice of a split unit.
+  {
+    std::vector<int32_t> pair_total((size_t)B * n_kv_heads, 0);
+    auto pair_of = [&](const Unit& U) {
+      const int bt = U.bt_g / n_kv_heads;
+      return (size_t)(bt / T) * n_kv_heads + (U.bt_g - bt * n_kv_heads);
+    };
+    for (const Unit& U : units)
+      pair_total[pair_of(U)] += U.n_parts > 1 ? split_slices(U.n_parts) : 1;
+    for (Unit& U : units) U.pair_total = pair_total[pair_of(U)];
+  }
+  for (const Launch& L : launches) {
+    common.n_requests = L.u0 == 0 ? B : 0;   // new rows are stored by the first launch
     int rc;
-    if (n <= (size_t)kMaxUnitsSmall) {
-      rc = tensor_cores ? launch_units<kMaxUnitsSmall, true>(tmap, units, u0, n, eff_total, grid,
-                                                             common, stream)
-                        : launch_units<kMaxUnitsSmall, false>(tmap, units, u0, n, eff_total,
-                                                              grid, common, stream);
+    if (L.n <= (size_t)kMaxUnitsSmall) {
+      rc = tensor_cores ? launch_units<kMaxUnitsSmall, true>(tmap, units, L.u0, L.n, L.total,
+                                                             L.grid, common, stream)
+                        : launch_units<kMaxUnitsSmall, false>(tmap, units, L.u0, L.n, L.total,
+                                                              L.grid, common, stream);
     } else {
-      rc = tensor_cores ? launch_units<kMaxUnitsLarge, true>(tmap, units, u0, n, eff_total, grid,
-                                                             common, stream)
-                        : launch_units<kMaxUnitsLarge, false>(tmap, units, u0, n, eff_total,
-                                                              grid, common, stream);
+      rc = tensor_cores ? launch_units<kMaxUnitsLarge, true>(tmap, units, L.u0, L.n, L.total,
+                                                             L.grid, common, stream)
+                        : launch_units<kMaxUnitsLarge, false>(tmap, units, L.u0, L.n, L.total,
+                                                              L.grid, common, stream);
     }
     if (rc != PA_OK) return rc;
   }

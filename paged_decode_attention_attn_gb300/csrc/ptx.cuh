@@ -103,6 +103,32 @@ __device__ __forceinline__ int atomic_add_acq_rel_gpu(int* p, int v) {
                : "memory");
   return old;
 }
+__device__ __forceinline__ unsigned long long atomic_add_acq_rel_gpu(unsigned long long* p,
+                                                                     unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.add.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
+// Device-scope add whose result is not needed, with release semantics.
+__device__ __forceinline__ void red_add_release_gpu(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long load_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ unsigned long long atomic_cas_gpu(unsigned long long* p,
+                                                             unsigned long long expected,
+                                                             unsigned long long desired) {
+  unsigned long long old;
+  asm volatile("atom.relaxed.gpu.global.cas.b64 %0, [%1], %2, %3;"
+               : "=l"(old)
+               : "l"(p), "l"(expected), "l"(desired)
+               : "memory");
+  return old;
+}
 __device__ __forceinline__ void prefetch_tensormap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
