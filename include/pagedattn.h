@@ -366,11 +366,13 @@ typedef struct {
 
 typedef struct {
     uint64_t stage_generation;  /* stages begun so far; strictly increasing     */
-    uint64_t staged_bytes;      /* bytes enqueued host->device                   */
+    uint64_t staged_bytes;      /* bytes enqueued host->device by stages/leases  */
     uint64_t written_back_bytes;/* bytes enqueued device->host                   */
     uint64_t slot_reuses;       /* stages that had to wait on a slot's readers   */
     int32_t  quarantined;       /* 1 after any failure                           */
     int32_t  n_slots;
+    uint64_t loaded_bytes;      /* bytes enqueued host->device by kv_load_resident
+                                   (not in staged_bytes)                         */
 } kv_arena_stats;
 
 /* Create an arena over caller memory.  Creates one copy, attention and
@@ -413,6 +415,34 @@ int kv_mark_attention_done(kv_arena* arena, int layer);
  * enqueued) an owner other than the one the layer was staged with. */
 int kv_writeback_tail(kv_arena* arena, int layer, const kv_tail_req* reqs,
                       int n_reqs);
+
+/* One page (or its leading rows) copied into the arena's resident region. */
+typedef struct {
+    int64_t     resident_page;  /* arena page (relative to device_base) outside
+                                   the staging slots                            */
+    int32_t     n_rows;         /* rows copied into the page from its row 0,
+                                   1..page_tokens                               */
+    int32_t     pad_;
+    const void* host_rows;      /* pinned host source: n_rows consecutive rows  */
+} kv_resident_load;
+
+/* Copy-in of resident pages ([SWS-admit]; "GPU memory management", section
+ * "Pages held by right, borrowed or free": a page that turns hot is copied
+ * into the device pool once and then served from there): the initial fill of
+ * a static window, or the pages the admission planner made hot.  On the
+ * device, in this order: the H2D stream waits on the most recent attention
+ * and write-back events of this arena (their streams run in order, so every
+ * earlier attention and write-back that may read the pages being replaced is
+ * then done), one cudaMemcpyAsync per load, the arena's load event, and the
+ * compute stream's wait on it (attention enqueued after this call sees the
+ * pages; a later stage's copies follow them on the H2D stream).  The caller
+ * marks attention done (kv_mark_attention_done / kv_lease_attention_done)
+ * after every kernel that reads resident pages, as for staged ones.  Refused
+ * before anything is enqueued (PA_ERR_INVALID): a page inside the staging
+ * slots or outside the arena, n_rows outside 1..page_tokens, host rows not in
+ * pinned host memory.  A failed submission quarantines the arena.  Works with
+ * stage calls and with leases. */
+int kv_load_resident(kv_arena* arena, const kv_resident_load* loads, int n_loads);
 
 /* ------------------------------------------------------------------------ */
 /* Leases  ([SWS-lease], [KVE-lease], "GPU memory management" / "Staging as   */

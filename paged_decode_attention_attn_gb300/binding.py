@@ -42,7 +42,7 @@ EXPORTED = [
     "paged_decode_attn_lse_append", "paged_decode_attn_test_stall", "lse_merge",
     "kv_append_rows",
     "kv_arena_create", "kv_arena_destroy", "kv_arena_drain", "kv_stage_layer",
-    "kv_mark_attention_done", "kv_writeback_tail", "kv_arena_get_stats",
+    "kv_mark_attention_done", "kv_writeback_tail", "kv_load_resident", "kv_arena_get_stats",
     "kv_arena_fail_after", "kv_arena_call_log",
     "kv_lease_begin", "kv_lease_attention_done", "kv_lease_writeback", "kv_lease_seal",
     "kv_lease_retire", "kv_host_generation", "kv_host_recycle",
@@ -114,6 +114,15 @@ class KvTailReq(ctypes.Structure):
     ]
 
 
+class KvResidentLoad(ctypes.Structure):
+    _fields_ = [
+        ("resident_page", ctypes.c_int64),
+        ("n_rows", ctypes.c_int32),
+        ("pad_", ctypes.c_int32),
+        ("host_rows", ctypes.c_void_p),
+    ]
+
+
 class KvArenaStats(ctypes.Structure):
     _fields_ = [
         ("stage_generation", ctypes.c_uint64),
@@ -122,6 +131,7 @@ class KvArenaStats(ctypes.Structure):
         ("slot_reuses", ctypes.c_uint64),
         ("quarantined", ctypes.c_int32),
         ("n_slots", ctypes.c_int32),
+        ("loaded_bytes", ctypes.c_uint64),
     ]
 
 
@@ -239,6 +249,8 @@ def _load():
     lib.kv_mark_attention_done.argtypes = [vp, i32]
     lib.kv_writeback_tail.restype = i32
     lib.kv_writeback_tail.argtypes = [vp, i32, ctypes.POINTER(KvTailReq), i32]
+    lib.kv_load_resident.restype = i32
+    lib.kv_load_resident.argtypes = [vp, ctypes.POINTER(KvResidentLoad), i32]
     lib.kv_arena_get_stats.restype = i32
     lib.kv_arena_get_stats.argtypes = [vp, ctypes.POINTER(KvArenaStats)]
     lib.kv_arena_fail_after.restype = i32
@@ -527,6 +539,17 @@ class Arena:
 
     def mark_attention_done(self, layer: int):
         _check(lib.kv_mark_attention_done(self.handle, layer))
+
+    def load_resident(self, loads):
+        """loads: list of (resident_page, n_rows, host_rows_address)."""
+        if not loads:
+            return
+        arr = (KvResidentLoad * len(loads))()
+        for k, (page, n_rows, host) in enumerate(loads):
+            arr[k].resident_page = page
+            arr[k].n_rows = n_rows
+            arr[k].host_rows = host
+        _check(lib.kv_load_resident(self.handle, arr, len(loads)))
 
     def writeback_tail(self, layer: int, tails):
         """tails: list of (request, position, host_row_address, owner)."""

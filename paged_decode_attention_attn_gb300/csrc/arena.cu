@@ -168,6 +168,7 @@ struct Lease {
   uint64_t attention_token = 0;
   uint64_t writeback_token = 0;  // 0 until a write-back is issued
   uint64_t staged_bytes = 0;
+  uint64_t loaded_bytes = 0;      // kv_load_resident copies
   uint64_t written_back_bytes = 0;
   int32_t n_requests = 0;
   std::vector<Ticket> tickets;
@@ -190,10 +191,14 @@ struct kv_arena {
   int64_t fail_after = -1;
   std::string log;
   std::vector<cudaEvent_t> ev_copy, ev_attn, ev_wb;
+  cudaEvent_t ev_load = nullptr;  // recorded after each kv_load_resident's copies
+  int last_attn_slot = -1;        // slot of the most recent attention event
+  int last_wb_slot = -1;          // slot of the most recent write-back event
   std::vector<pa::arena::Slot> slots;
   std::map<int, int> layer_slot;
   uint64_t generation = 0;
   uint64_t staged_bytes = 0;
+  uint64_t loaded_bytes = 0;      // kv_load_resident copies
   uint64_t written_back_bytes = 0;
   uint64_t slot_reuses = 0;
   int64_t page_bytes = 0;
@@ -555,6 +560,7 @@ int submit_tails(kv_arena* a, int slot, const kv_tail_req* reqs, int n_reqs,
   }
   if ((rc = op_record(a, d.d2h_stream, "wb", slot, a->ev_wb[slot])) != PA_OK) return rc;
   a->slots[slot].written_back = true;
+  a->last_wb_slot = slot;
   return PA_OK;
 }
 
@@ -634,6 +640,8 @@ extern "C" int kv_arena_create(const kv_arena_desc* desc, kv_arena** out) {
       cudaError_t e = cudaEventCreateWithFlags(&a->ev_copy[s], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a->ev_attn[s], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&a->ev_wb[s], cudaEventDisableTiming);
+      if (e == cudaSuccess && s == 0)
+        e = cudaEventCreateWithFlags(&a->ev_load, cudaEventDisableTiming);
       if (e != cudaSuccess) {
         kv_arena_destroy(a);
         return fail(PA_ERR_CUDA, "cudaEventCreateWithFlags failed: %s", cudaGetErrorString(e));
@@ -651,6 +659,7 @@ extern "C" int kv_arena_destroy(kv_arena* a) {
   for (auto* v : {&a->ev_copy, &a->ev_attn, &a->ev_wb})
     for (cudaEvent_t e : *v)
       if (e) cudaEventDestroy(e);
+  if (a->ev_load) cudaEventDestroy(a->ev_load);
   delete a;
   return PA_OK;
 }
@@ -682,6 +691,8 @@ extern "C" int kv_arena_drain(kv_arena* a) {
   a->leases.clear();
   a->last_lease = 0;
   a->layer_slot.clear();
+  a->last_attn_slot = -1;
+  a->last_wb_slot = -1;
   a->quarantined = false;
   return PA_OK;
 }
@@ -734,6 +745,7 @@ extern "C" int kv_mark_attention_done(kv_arena* a, int layer) {
     return fail(PA_ERR_ORDER, "layer %d is not awaiting attention (slot %d)", layer, it->second);
   rc = op_record(a, a->d.compute_stream, "attn", it->second, a->ev_attn[it->second]);
   if (rc != PA_OK) return rc;
+  a->last_attn_slot = it->second;
   S.state = kAttended;
   return PA_OK;
 }
@@ -755,6 +767,59 @@ extern "C" int kv_writeback_tail(kv_arena* a, int layer, const kv_tail_req* reqs
   if ((rc = resolve_tails(a, slot, layer, reqs, n_reqs, &src)) != PA_OK) return rc;
   uint64_t bytes = 0;
   return submit_tails(a, slot, reqs, n_reqs, src, &bytes);
+}
+
+// ---------------------------------------------------------------------------
+// Copy-in of resident pages.
+// ---------------------------------------------------------------------------
+
+extern "C" int kv_load_resident(kv_arena* a, const kv_resident_load* loads, int n_loads) {
+  pa::clear_error();
+  PA_REQUIRE(a, "null arena");
+  if (a->quarantined) return fail(PA_ERR_QUARANTINED, "arena is quarantined; drain it first");
+  PA_REQUIRE(n_loads >= 0 && (n_loads == 0 || loads), "bad load list");
+  const kv_arena_desc& d = a->d;
+  const int64_t slots_end = d.slot_first_page + (int64_t)d.n_slots * d.slot_pages;
+  for (int i = 0; i < n_loads; ++i) {
+    const kv_resident_load& L = loads[i];
+    PA_REQUIRE(L.resident_page >= 0 && L.resident_page < a->arena_pages,
+               "load %d: page %" PRId64 " outside the arena's %" PRId64 " pages", i,
+               L.resident_page, a->arena_pages);
+    PA_REQUIRE(L.resident_page < d.slot_first_page || L.resident_page >= slots_end,
+               "load %d: page %" PRId64 " lies in the staging slots [%" PRId64 ", %" PRId64 ")",
+               i, L.resident_page, d.slot_first_page, slots_end);
+    PA_REQUIRE(L.n_rows >= 1 && L.n_rows <= d.page_tokens, "load %d: n_rows %d outside 1..%d", i,
+               L.n_rows, d.page_tokens);
+    PA_REQUIRE(L.host_rows != nullptr, "load %d: null host rows", i);
+    if (!a->record_only) {
+      cudaPointerAttributes attr;
+      const cudaError_t e = cudaPointerGetAttributes(&attr, L.host_rows);
+      PA_REQUIRE(e == cudaSuccess && attr.type == cudaMemoryTypeHost,
+                 "load %d: host rows must be pinned host memory", i);
+    }
+  }
+  if (n_loads == 0) return PA_OK;
+  const cudaStream_t h2d = d.h2d_stream;
+  int rc;
+  // The pages being replaced may still be read by earlier attention (through
+  // a page table) or by a tail write-back (the new row of a resident page).
+  if (a->last_attn_slot >= 0 &&
+      (rc = op_wait(a, h2d, "attn", a->last_attn_slot, a->ev_attn[a->last_attn_slot])) != PA_OK)
+    return rc;
+  if (a->last_wb_slot >= 0 &&
+      (rc = op_wait(a, h2d, "wb", a->last_wb_slot, a->ev_wb[a->last_wb_slot])) != PA_OK)
+    return rc;
+  uint8_t* base = static_cast<uint8_t*>(d.device_base);
+  for (int i = 0; i < n_loads; ++i) {
+    const kv_resident_load& L = loads[i];
+    const size_t nb = (size_t)L.n_rows * d.row_bytes;
+    if ((rc = op_copy(a, h2d, base + L.resident_page * a->page_bytes, L.host_rows, nb,
+                      cudaMemcpyHostToDevice, L.resident_page, 0)) != PA_OK)
+      return rc;
+    a->loaded_bytes += nb;
+  }
+  if ((rc = op_record(a, h2d, "load", 0, a->ev_load)) != PA_OK) return rc;
+  return op_wait(a, d.compute_stream, "load", 0, a->ev_load);
 }
 
 // ---------------------------------------------------------------------------
@@ -835,6 +900,7 @@ extern "C" int kv_lease_attention_done(kv_arena* a, uint64_t lease_id, uint64_t*
     return fail(PA_ERR_ORDER, "lease %" PRIu64 " already has its attention event", lease_id);
   const int rc = op_record(a, a->d.compute_stream, "attn", L->slot, a->ev_attn[L->slot]);
   if (rc != PA_OK) return rc;
+  a->last_attn_slot = L->slot;
   L->state = kLeaseAttended;
   L->attention_token = ++a->event_tokens;
   a->slots[L->slot].state = kAttended;
@@ -950,6 +1016,7 @@ extern "C" int kv_arena_get_stats(const kv_arena* a, kv_arena_stats* out) {
   out->slot_reuses = a->slot_reuses;
   out->quarantined = a->quarantined ? 1 : 0;
   out->n_slots = a->d.n_slots;
+  out->loaded_bytes = a->loaded_bytes;
   return PA_OK;
 }
 

@@ -339,11 +339,6 @@ class StagedDecode:
         self.arena = self.arena_buf[: arena_pages * page_bytes].view(torch.bfloat16).view(
             arena_pages, pt, geo.row_elems)
         self.arena.fill_(float("nan"))          # canary: unwritten rows read as NaN
-        for (i, r), wb in win_base.items():     # resident window copied in once
-            n = w.pages_of(r)
-            idx = list(range(sink)) + list(range(n - recent, n))
-            phys = torch.as_tensor(w.page_table[r, idx], dtype=torch.long, device=dev)
-            self.arena[wb:wb + sink + recent] = t["pool"][i].index_select(0, phys)
         self.page_tables = torch.zeros((n_slots, w.batch, w.max_pages), dtype=torch.int32,
                                        device=dev)
         torch.cuda.synchronize(dev)
@@ -354,6 +349,16 @@ class StagedDecode:
                               compact_head_dim=geo.head_dim if compact is not None else 0,
                               landing_offset=arena_pages * page_bytes if landing else 0,
                               landing_bytes=landing)
+        # The resident window is copied in once, from the pinned host history
+        # (the new token's row comes from the step's own tail write).
+        loads = []
+        for (i, r), wb in win_base.items():
+            n, L = w.pages_of(r), int(w.lengths[r])
+            for k, lp in enumerate(list(range(sink)) + list(range(n - recent, n))):
+                rows = min(L - 1, (lp + 1) * pt) - lp * pt
+                if rows > 0:
+                    loads.append((wb + k, rows, host.row_address(i, r, lp * pt)))
+        self.handle.load_resident(loads)
         self.exact_plan = self.plan
         if compact is not None:
             self.replan()
@@ -632,9 +637,10 @@ class PlannedDecode:
     staging slots.  At each step the planner decides every context's hot
     pages ("Staging without a stall", section "Admission that does
     arithmetic"); pages that turned hot are copied in once from pinned host
-    memory (after the previous step's attention and write-back are done with
-    the pool pages they reuse), and each layer stages every page that is not
-    hot.  Contexts are the workload's requests; all run every step.
+    memory by the arena (kv_load_resident: after the previous step's
+    attention and write-back are done with the pool pages they reuse), and
+    each layer stages every page that is not hot.  Contexts are the
+    workload's requests; all run every step.
 
     With a CompactStore, the hot window stays exact and every cold page that
     the background converter has published is staged compact ("KV-cache
@@ -685,9 +691,6 @@ class PlannedDecode:
                               landing_bytes=landing)
         for r in range(w.batch):
             planner.admit(r, int(targets[r]), int(bursts[r]))
-        self.step_done = torch.cuda.Event()
-        self.wb_done = torch.cuda.Event()
-        self.have_prev = False
         self.status = torch.zeros(1, dtype=torch.int32, device=dev)
         self.workspace = B.alloc_workspace(w.batch, 1, geo.n_q_heads, geo.n_kv_heads,
                                            geo.head_dim, device=dev)
@@ -701,25 +704,22 @@ class PlannedDecode:
         self.resident = [dict() for _ in range(w.batch)]
 
     def _copy_in(self, lengths):
-        """Copy the pages that turned hot into their pool pages, every layer."""
-        geo = self.w.geometry
-        pt = geo.page_tokens
-        if self.have_prev:
-            self.h2d.wait_event(self.step_done)
-            self.h2d.wait_event(self.wb_done)
-        with torch.cuda.stream(self.h2d):
-            for r in range(self.w.batch):
-                res = self.resident[r]
-                for lp in self.planner.copied(r):
-                    lo = lp * pt
-                    hi = min(int(lengths[r]) - 1, lo + pt)   # the new row comes from append
-                    if hi <= lo:
-                        continue
-                    for i in range(self.n_layers):
-                        page = i * self.pool_pages + res[lp]
-                        src = self.host.rows[self.host.offsets[(i, r)] + lo:
-                                             self.host.offsets[(i, r)] + hi]
-                        self.arena[page, : hi - lo].copy_(src, non_blocking=True)
+        """Copy the pages that turned hot into their pool pages, every layer
+        (one kv_load_resident call: ordered after the previous step's
+        attention and write-backs, which may read the pool pages reused)."""
+        pt = self.w.geometry.page_tokens
+        loads = []
+        for r in range(self.w.batch):
+            res = self.resident[r]
+            for lp in self.planner.copied(r):
+                lo = lp * pt
+                rows = min(int(lengths[r]) - 1, lo + pt) - lo   # the new row comes from append
+                if rows <= 0:
+                    continue
+                for i in range(self.n_layers):
+                    loads.append((i * self.pool_pages + res[lp], rows,
+                                  self.host.row_address(i, r, lo)))
+        self.handle.load_resident(loads)
 
     def _runs(self, i, r, L, published=None):
         """Page runs of request r for layer i: hot pages from the pool,
@@ -787,9 +787,6 @@ class PlannedDecode:
             self.handle.writeback_tail(
                 i, [(r, int(lengths[r]) - 1, self.host.row_address(i, r, int(lengths[r]) - 1),
                      (i << 32) | r) for r in range(w.batch)])
-        self.step_done.record(self.compute)
-        self.wb_done.record(self.d2h)
-        self.have_prev = True
         if self.compact is not None:
             ev = torch.cuda.Event()
             ev.record(self.d2h)

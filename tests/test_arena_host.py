@@ -277,3 +277,74 @@ def test_landing_geometry_is_checked(B):
     with pytest.raises(B.PagedAttnError):          # head_dim does not divide the row
         B.Arena(BASE, 40 * PAGE * ROW, ROW, 2, 4, 8, TABLES, 4, 16, record_only=True,
                 compact_head_dim=96, landing_offset=20 * PAGE * ROW, landing_bytes=CPAGE)
+
+
+# ---- copy-in of resident pages ("Staging without a stall", section
+# "Admission that does arithmetic"; "GPU memory management", section "Pages
+# held by right, borrowed or free": a page that turns hot is copied in once) ----
+
+def test_load_resident_orders_compute_after_the_copies(B):
+    a = make_arena(B, window_pages=4)
+    a.load_resident([(0, 64, 0x1000), (3, 17, 0x9000)])
+    assert a.call_log() == [
+        "h2d copy h2d bytes=262144 page=0 row=0",
+        "h2d copy h2d bytes=69632 page=3 row=0",
+        "h2d record load[0]",
+        "compute wait load[0]",
+    ]
+    assert a.stats().loaded_bytes == (64 + 17) * ROW and a.stats().staged_bytes == 0
+
+
+def test_load_resident_waits_on_the_latest_readers(B):
+    a = make_arena(B, n_slots=2, window_pages=4)
+    full_layer(B, a, 0, [(0, 1, [resident(0, 1, 0), staged(1, 1, 0x1000, rows=10)])],
+               [(0, 73, 0x5000, 1)])
+    a.stage_layer(1, [(0, 1, [resident(0, 1, 0), staged(1, 1, 0x2000, rows=10)])])
+    a.mark_attention_done(1)            # layer 1: attention, no write-back yet
+    n = len(a.call_log())
+    a.load_resident([(0, 64, 0x3000)])
+    assert a.call_log()[n:] == [
+        "h2d wait attn[1]",             # the latest attention (covers layer 0's)
+        "h2d wait wb[0]",               # the latest write-back
+        "h2d copy h2d bytes=262144 page=0 row=0",
+        "h2d record load[0]",
+        "compute wait load[0]",
+    ]
+    a.drain()
+    n = len(a.call_log())
+    a.load_resident([(1, 64, 0x3000)])  # after a drain nothing is pending
+    assert a.call_log()[n:][0] == "h2d copy h2d bytes=262144 page=1 row=0"
+
+
+def test_load_resident_is_checked_before_anything_is_enqueued(B):
+    a = make_arena(B, n_slots=2, slot_pages=8, window_pages=4)
+    bad = [
+        [(4, 64, 0x1000)],                # slot 0's first page
+        [(19, 1, 0x1000)],                # inside slot 1
+        [(20, 1, 0x1000)],                # past the arena
+        [(-1, 1, 0x1000)],
+        [(0, 0, 0x1000)],                 # no rows
+        [(0, 65, 0x1000)],                # more rows than a page
+        [(0, 64, 0)],                     # null host rows
+        [(0, 64, 0x1000), (5, 64, 0x2000)],  # one bad load refuses the call
+    ]
+    for loads in bad:
+        with pytest.raises(B.PagedAttnError) as e:
+            a.load_resident(loads)
+        assert e.value.code == B.PA_ERR_INVALID
+    assert a.call_log() == []
+    assert a.stats().loaded_bytes == 0
+
+
+@pytest.mark.parametrize("fail_at", range(0, 4))
+def test_load_resident_failure_quarantines(B, fail_at):
+    a = make_arena(B)
+    a.fail_after(fail_at)
+    with pytest.raises(B.PagedAttnError) as e:
+        a.load_resident([(0, 64, 0x1000), (1, 64, 0x2000)])
+    assert e.value.code == B.PA_ERR_CUDA
+    with pytest.raises(B.PagedAttnError) as e:
+        a.load_resident([(0, 64, 0x1000)])
+    assert e.value.code == B.PA_ERR_QUARANTINED
+    a.drain()
+    a.load_resident([(0, 64, 0x1000)])

@@ -1,8 +1,9 @@
 """Race checks of the staging arena's device ordering, on the CPU.
 
-Record-only arenas are driven through seeded random stage and lease sessions
-(staged, resident and compact runs, one to three slots, write-back or not),
-the way the decode routes drive them; the happens-before checker in
+Record-only arenas are driven through seeded random stage, lease and
+planner sessions (staged, resident and compact runs, copy-ins of resident
+pages, one to three slots, write-back or not), the way the decode routes
+drive them; the happens-before checker in
 ``event_order.py`` replays each log against the CUDA stream and event rules
 and must find no race.  The checker is pinned first by hand-written logs and
 then by planted mistakes: every wait, and every copy record, dropped from a
@@ -260,3 +261,80 @@ def test_dropped_host_waits_are_flagged_when_they_order_a_refill(B):
     assert flagged >= 1
     stripped = [line for line in log if not line.startswith("host wait")]
     assert E.races(stripped)
+
+
+# ---- copy-in of resident pages (the planner's hot pages, a static window) ----
+
+def planner_session(B, seed, n_slots, n_layers=3, steps=4, n_req=2, pool_pages=3):
+    """Each step copies a random set of pool pages in (kv_load_resident), then
+    stages every layer with runs mapping pool pages of its own region and a
+    staged run, tails in either; write-backs on random layers."""
+    rng = np.random.default_rng(seed)
+    a = make_arena(B, n_slots, n_layers * pool_pages, False)
+    for step in range(steps):
+        loads = []
+        for layer in range(n_layers):
+            for p in range(pool_pages):
+                if rng.random() < 0.5:
+                    loads.append((layer * pool_pages + p, int(rng.integers(1, PAGE + 1)),
+                                  0x20000000 + 0x100000 * (step * 16 + layer * pool_pages + p)))
+        a.load_resident(loads)
+        for layer in range(n_layers):
+            reqs, tails = [], []
+            for r in range(n_req):
+                p = int(rng.integers(0, pool_pages))
+                runs = [dict(logical_page=0, n_pages=1, resident_page=layer * pool_pages + p),
+                        dict(logical_page=1, n_pages=1, n_rows=int(rng.integers(1, PAGE + 1)),
+                             host_rows=0x10000000 * (layer + 1) + 0x1000000 * r)]
+                tail = int(rng.integers(0, 2 * PAGE))
+                reqs.append((r, 100 + r, runs))
+                tails.append((r, tail, 0x7000000 + 0x10000 * layer + r, 100 + r))
+            a.stage_layer(layer, reqs)
+            a.mark_attention_done(layer)
+            if rng.random() < 0.7:
+                a.writeback_tail(layer, tails)
+    return a.call_log()
+
+
+@pytest.mark.parametrize("n_slots", [1, 2, 3])
+@pytest.mark.parametrize("seed", range(4))
+def test_planner_sessions_have_no_race(B, seed, n_slots):
+    log = planner_session(B, seed, n_slots)
+    assert any("record load" in line for line in log)
+    assert E.races(log) == []
+
+
+def fixed_load_session(B, steps=3):
+    """Every step reloads pool page 0, which both layers map and whose row 10
+    holds the new token (stored by the attention, read by the write-back),
+    between layer 0's stage and its attention; only layer 0 writes back.
+    Three slots, so some loads follow a stage that waited on nothing."""
+    a = make_arena(B, 3, 1, False)
+    for step in range(steps):
+        for layer in range(2):
+            runs = [dict(logical_page=0, n_pages=1, resident_page=0),
+                    dict(logical_page=1, n_pages=1, n_rows=40,
+                         host_rows=0x10000000 * (layer + 1))]
+            a.stage_layer(layer, [(0, 100, runs)])
+            if layer == 0:
+                a.load_resident([(0, PAGE, 0x20000000 + 0x100000 * step)])
+            a.mark_attention_done(layer)
+            if layer == 0:
+                a.writeback_tail(layer, [(0, 10, 0x7000000 + layer, 100)])
+    return a.call_log()
+
+
+def test_every_kind_of_load_wait_and_record_guards_bytes(B):
+    log = fixed_load_session(B)
+    assert E.races(log) == []
+    loads = [i for i, line in enumerate(log) if line.startswith("h2d copy") and "page=0 " in line]
+    assert len(loads) == 3
+    flagged = set()
+    for c in loads:
+        # the load's own lines: the waits just before its copy, its record and
+        # the compute wait just after it
+        own = [c + 1, c + 2] + [j for j in (c - 1, c - 2) if log[j].startswith("h2d wait")]
+        for i in own:
+            if E.races(log[:i] + log[i + 1:]):
+                flagged.add(log[i].split("[")[0])
+    assert flagged == {"h2d record load", "compute wait load", "h2d wait attn", "h2d wait wb"}

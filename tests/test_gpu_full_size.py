@@ -103,6 +103,16 @@ def test_staged_route_is_bit_identical_to_resident(D, name, n_slots, leases):
     st = staged.handle.stats()
     assert st.stage_generation == w.n_layers and st.quarantined == 0
     assert st.written_back_bytes == w.n_layers * w.batch * w.geometry.row_bytes
+    # the resident window came from the pinned host rows: the sink page and
+    # the newest pages up to (not including) the new token's row
+    window_rows = 0
+    if w.window:
+        sink, recent = w.window
+        for r in range(w.batch):
+            n, L = w.pages_of(r), int(w.lengths[r])
+            if n > sink + recent:
+                window_rows += sink * 64 + (L - 1) - (n - recent) * 64
+    assert st.loaded_bytes == w.n_layers * window_rows * w.geometry.row_bytes
     if leases:
         assert [r.layer for r in staged.receipts] == list(range(w.n_layers))
         assert sum(r.staged_bytes for r in staged.receipts) == st.staged_bytes
