@@ -68,3 +68,24 @@ def test_timeline_reading_names_the_bound():
                                                     "host_gap": 0.25},
                                 "copy_GBps": {"median": 210.0, "min": 200.0}})
     assert "waiting for the host" in r and "25.0%" in r
+
+
+def test_timeline_accounts_for_stages_that_copied_slowly():
+    # 1 slot, 10 MB per stage: three stages at 10 GB/s (1 ms) and one at
+    # 2.5 GB/s (4 ms): one slow stage, 3 ms beyond the fastest stage's rate.
+    ev = [
+        stage(0.0, 1.0, 1.0, 1.1, 1.2),
+        stage(1.2, 2.2, 2.2, 2.3, 2.4),
+        stage(2.4, 6.4, 6.4, 6.5, 6.6),
+        stage(6.6, 7.6, 7.6, 7.7, 7.8),
+    ]
+    r = bench.timeline_stats(ev, 1, [10_000_000], steps=2)
+    slow = r["slow_stages"]
+    assert slow["n"] == 1 and slow["of"] == 4
+    assert slow["fastest_stage_GBps"] == pytest.approx(10.0)
+    assert slow["below_GBps"] == pytest.approx(9.0)
+    assert slow["rates_GBps"] == [2.5]
+    assert slow["excess_ms_per_step"] == pytest.approx(1.5)     # 3 ms over 2 steps
+    r["h2d_time_split"] = {"copying": 0.99, "slot_wait": 0.0, "host_gap": 0.01}
+    text = bench.timeline_reading(r)
+    assert "1 of 4 stages" in text and "1.5 ms" in text

@@ -45,3 +45,24 @@ def test_degenerate_inputs_are_refused():
 
 def test_staged_bytes_counts_history_without_the_new_row():
     assert bm.staged_bytes_per_step([31744] * 4, 16, 4096) == 4 * 31743 * 4096 * 16
+
+
+def test_bench_predictions_use_single_steps_on_a_free_link():
+    import os
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    import bench
+    model = bm.BusModel(fixed_s=0.001, link_bytes_per_s=200e9)
+    legs = {"a": {"staged_bytes_per_step": 2_000_000_000,          # predicts 11 ms
+                  "pairs": {"step_ms": [11.0, 40.0, 11.5, 30.0], "step_ms_median": 20.75,
+                            "stage_min_GBps": [210.0, 60.0, 205.0, 80.0]}},
+            "b": {"staged_bytes_per_step": 1_000_000_000,
+                  "pairs": {"step_ms": [50.0], "step_ms_median": 50.0,
+                            "stage_min_GBps": [50.0]}}}
+    out = bench.bus_predictions(model, legs, best_stage=211.0)
+    a = out["per_leg"]["a"]
+    assert a["pairs_used"] == 2 and a["measured_ms"] == 11.25          # the two free-link pairs
+    assert a["predicted_ms"] == 11.0
+    assert a["error_pct"] == round(100 * (11.0 - 11.25) / 11.25, 3)
+    assert out["per_leg"]["b"]["pairs_used"] == 0                       # no free-link pair
+    assert out["worst_abs_error_pct"] == abs(a["error_pct"])
