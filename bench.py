@@ -714,31 +714,33 @@ def null_arm(args, w, t, D, B, dev, fused, kv_ready):
     return e0.elapsed_time(e1) / n
 
 
-def merge_arm(dev, B, iters=50):
+def merge_arm(dev, B, iters=50, copies=4):
     """The standalone FP32 LSE merge on the merge-stress shape: 64 requests x
     24 heads x 256, 1..64 partials per request, partial LSEs spread +-80.  The
-    partials (~51 MB) fit in L2, so a 256 MiB buffer is written before every
-    launch; each launch is timed alone with CUDA events on its stream."""
+    partials (~51 MB) fit in L2, so the launches cycle through ``copies``
+    copies of them (~205 MB, larger than L2): each launch reads partials that
+    the previous launches evicted from L2, without a flush whose dirty lines
+    would be written back during the launch.  Each launch is timed alone with
+    CUDA events on its stream."""
     import torch
     from paged_decode_attention_attn_gb300 import workloads as wl
     H, Dh = 24, 256
     offsets = wl.merge_stress_layout()
-    out_parts, lse_parts = wl.merge_stress_partials_device(offsets, H, Dh, dev)
+    parts = [wl.merge_stress_partials_device(offsets, H, Dh, dev) for _ in range(copies)]
     n_req = len(offsets) - 1
     off_d = torch.as_tensor(offsets, dtype=torch.int32).to(dev)
     out = torch.empty((n_req, H, Dh), dtype=torch.float32, device=dev)
     lse = torch.empty((n_req, H), dtype=torch.float32, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(iters)]
-    for _ in range(3):
-        B.lse_merge(out_parts, lse_parts, off_d, out, lse, stream=stream)
+    for k in range(2 * copies):
+        B.lse_merge(parts[k % copies][0], parts[k % copies][1], off_d, out, lse, stream=stream)
     torch.cuda.synchronize(dev)
-    for e0, e1 in ev:
-        flush.fill_(1)
+    for k, (e0, e1) in enumerate(ev):
+        op, lp = parts[k % copies]
         e0.record(stream)
-        B.lse_merge(out_parts, lse_parts, off_d, out, lse, stream=stream)
+        B.lse_merge(op, lp, off_d, out, lse, stream=stream)
         e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = statistics.median(e0.elapsed_time(e1) for e0, e1 in ev)
@@ -751,7 +753,8 @@ def merge_arm(dev, B, iters=50):
             "median_launch_us": round(ms * 1e3, 2), "launches": iters,
             "bytes_per_launch": nbytes, "partials": n_parts, "requests": n_req,
             "frac_of_hbm_peak": round(gbs / peak, 4), "peak_kind": peak_kind,
-            "l2": "256 MiB buffer written before every launch (partials fit in L2)",
+            "l2": f"launches cycle through {copies} copies of the partials "
+                  f"({round(copies * nbytes / 1e6)} MB, larger than L2)",
             "workload": "64 requests x 24 heads x 256, 1..64 partials each, LSE +-80"}
 
 
