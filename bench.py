@@ -67,7 +67,7 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", choices=["4x31744", "1x262144", "ragged", "uniform"],
+    ap.add_argument("--workload", choices=["4x31744", "1x262144", "ragged", "1x32768", "uniform"],
                     default="4x31744",
                     help="4x31744 is the benchmarked workload; the others report the same "
                          "metric for the 262K-token and ragged-window workloads, or for "
