@@ -260,6 +260,15 @@ int paged_decode_attn_lse_append(const void* q, void* pool, int64_t pool_pages,
  * production calls never stall. */
 int paged_decode_attn_test_stall(int iteration, uint64_t wait_limit_ns);
 
+/* Test hook for the split-unit merge (no counterpart in the source pages):
+ * the next decode call made on this thread waits at most slice_wait_ns
+ * (instead of 50 us) without seeing another CTA of a split unit arrive
+ * before it leaves its merge slice to the unit's last CTA, so a test can
+ * drive the path that a grid not resident all at once takes; results are the
+ * same bits either way.  -1 clears a pending setting; PA_ERR_INVALID outside
+ * [-1, 50 us].  Production calls never use it. */
+int paged_decode_attn_test_slice_wait(int64_t slice_wait_ns);
+
 /* ------------------------------------------------------------------------ */
 /* FP32 LSE merge  ([KVE-exact])                                            */
 /* ------------------------------------------------------------------------ */

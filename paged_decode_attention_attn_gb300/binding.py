@@ -39,7 +39,8 @@ EXPORTED = [
     "kv_last_error", "pa_version", "kv_host_alloc", "kv_host_free",
     "paged_decode_attn_lse_workspace_bytes", "paged_decode_attn_lse",
     "paged_decode_attn_lse_cuda_core", "paged_decode_attn_lse_noalloc",
-    "paged_decode_attn_lse_append", "paged_decode_attn_test_stall", "lse_merge",
+    "paged_decode_attn_lse_append", "paged_decode_attn_test_stall",
+    "paged_decode_attn_test_slice_wait", "lse_merge",
     "kv_append_rows",
     "kv_arena_create", "kv_arena_destroy", "kv_arena_drain", "kv_stage_layer",
     "kv_mark_attention_done", "kv_writeback_tail", "kv_load_resident", "kv_arena_get_stats",
@@ -233,6 +234,8 @@ def _load():
                                                  vp, sz, ctypes.c_uint, vp]
     lib.paged_decode_attn_test_stall.restype = i32
     lib.paged_decode_attn_test_stall.argtypes = [i32, ctypes.c_uint64]
+    lib.paged_decode_attn_test_slice_wait.restype = i32
+    lib.paged_decode_attn_test_slice_wait.argtypes = [i64]
     lib.lse_merge.restype = i32
     lib.lse_merge.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
     lib.kv_append_rows.restype = i32
@@ -455,6 +458,13 @@ def test_stall(iteration: int, wait_limit_ns: int):
     """Failure-detection test hook: the next decode call on this thread stalls
     CTA 0 at page load ``iteration`` and gives waits up after wait_limit_ns."""
     _check(lib.paged_decode_attn_test_stall(int(iteration), int(wait_limit_ns)))
+
+
+def test_slice_wait(slice_wait_ns: int):
+    """Split-merge test hook: the next decode call on this thread waits at most
+    slice_wait_ns for another arrival before a CTA leaves its merge slice to
+    the unit's last CTA (-1 clears)."""
+    _check(lib.paged_decode_attn_test_slice_wait(int(slice_wait_ns)))
 
 
 def lse_merge(out_parts, lse_parts, part_offsets, out, lse, stream=None):

@@ -156,6 +156,10 @@ struct Params {
   // stage unarmed, so its consumers' wait runs out.
   unsigned long long wait_limit_ns;
   int stall_iteration;
+  // How long a split unit's CTA waits without a new arrival before it
+  // leaves its merge slice to the unit's last CTA (kSliceWaitNs; a test hook
+  // can shorten it to exercise that path).
+  unsigned long long slice_wait_ns;
   // Optional fused cross-tile merge: merged [B][Hq][kD] and [B][Hq].
   float* m_out;
   float* m_lse;
@@ -407,8 +411,8 @@ __device__ __forceinline__ void merge_split_slice(const Params<kMaxUnits>& p, in
 // returns false.  A CTA that finds every CTA arrived keeps waiting (the
 // opening follows the last arrival directly), up to wait_limit_ns.
 __device__ __forceinline__ bool wait_unit_complete(unsigned long long* arrival, unsigned gen,
-                                                   int n, uint64_t wait_limit_ns,
-                                                   int32_t* status) {
+                                                   int n, uint64_t slice_wait_ns,
+                                                   uint64_t wait_limit_ns, int32_t* status) {
   const uint64_t t0 = ptx::globaltimer_ns();
   uint64_t t_seen = t0;
   int seen = -1;
@@ -422,7 +426,7 @@ __device__ __forceinline__ bool wait_unit_complete(unsigned long long* arrival, 
       t_seen = now;
     }
     if (count < n) {
-      if (now - t_seen > kSliceWaitNs && ptx::atomic_cas_gpu(arrival, v, v + (1ull << 16)) == v)
+      if (now - t_seen > slice_wait_ns && ptx::atomic_cas_gpu(arrival, v, v + (1ull << 16)) == v)
         return false;
     } else if (now - t0 > wait_limit_ns) {
       atomicOr(status, PA_STATUS_TIMEOUT);
@@ -1034,8 +1038,8 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
           mode = leavers ? 2 : (participant ? 1 : 0);
           if (leavers) atomicAdd(p.status + 1, leavers);   // diagnostic count, not an error
         } else if (participant) {
-          mode = wait_unit_complete(arrival, (unsigned)(prev >> 32), n, p.wait_limit_ns,
-                                    p.status) ? 1 : 0;
+          mode = wait_unit_complete(arrival, (unsigned)(prev >> 32), n, p.slice_wait_ns,
+                                    p.wait_limit_ns, p.status) ? 1 : 0;
         }
         sh.merge_info[0] = mode;
         sh.merge_info[1] = leavers;
@@ -1146,6 +1150,7 @@ int launch_units(const CUtensorMap& tmap, const std::vector<Unit>& units, size_t
 // on the calling thread.
 thread_local int t_stall_iteration = -1;
 thread_local unsigned long long t_wait_limit_ns = 0;
+thread_local long long t_slice_wait_ns = -1;   // < 0: kSliceWaitNs
 
 // Every host-side check of a decode call; enqueues nothing and touches no
 // device state.  B * T == 0 passes (the call is then a no-op).
@@ -1274,8 +1279,10 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
   common.m_lse = merged_lse;
   common.wait_limit_ns = t_wait_limit_ns ? t_wait_limit_ns : kWaitLimitNs;
   common.stall_iteration = t_stall_iteration;
+  common.slice_wait_ns = t_slice_wait_ns >= 0 ? (unsigned long long)t_slice_wait_ns : kSliceWaitNs;
   t_stall_iteration = -1;
   t_wait_limit_ns = 0;
+  t_slice_wait_ns = -1;
 
   // Launches of at most kMaxUnitsLarge units each; every launch partitions its
   // own pages and reuses the workspace after the previous one (same stream).
@@ -1544,6 +1551,15 @@ extern "C" int paged_decode_attn_lse_noalloc(const void* q, const void* pool, in
     if (c != cudaSuccess)
       return pa::fail(PA_ERR_CUDA, "copying the status word failed: %s", cudaGetErrorString(c));
   }
+  return PA_OK;
+}
+
+extern "C" int paged_decode_attn_test_slice_wait(int64_t slice_wait_ns) {
+  pa::clear_error();
+  if (slice_wait_ns < -1 || slice_wait_ns > (int64_t)pa::decode::kSliceWaitNs)
+    return pa::fail(PA_ERR_INVALID, "slice_wait_ns must be -1 (clear) or in [0, %llu]",
+                    (unsigned long long)pa::decode::kSliceWaitNs);
+  pa::decode::t_slice_wait_ns = slice_wait_ns;
   return PA_OK;
 }
 

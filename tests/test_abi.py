@@ -149,3 +149,10 @@ def test_stall_hook_argument_checks(B):
     # a valid setting applies to the next call on this thread only; clear it
     assert B.lib.paged_decode_attn_test_stall(2, 50_000_000) == B.PA_OK
     assert B.lib.paged_decode_attn_test_stall(-1, 0) == B.PA_OK
+
+
+def test_slice_wait_hook_argument_checks(B):
+    assert B.lib.paged_decode_attn_test_slice_wait(-2) == B.PA_ERR_INVALID
+    assert B.lib.paged_decode_attn_test_slice_wait(50_001) == B.PA_ERR_INVALID
+    assert B.lib.paged_decode_attn_test_slice_wait(0) == B.PA_OK
+    assert B.lib.paged_decode_attn_test_slice_wait(-1) == B.PA_OK
