@@ -24,15 +24,16 @@ namespace merge {
 // kCols-column pass.  The row's partials stream through kStages shared-memory
 // stages of kStageParts partials each, filled by cp.async (16 bytes of a
 // partial's output row and 4 bytes of its LSE per copy), so the loads in
-// flight hold no registers.  Small stages keep a block's shared memory at
-// 16 KB, so a launch of ~1,500 rows runs in one wave (16-partial stages, six
-// blocks per SM, took two waves and measured 11% slower on the merge-stress
-// shape).  Every column sums its partials in increasing order with the same
-// expressions as the decode kernel's fused merge (mergerow::merge_cols), so
-// the bits are the same.
+// flight hold no registers.  Two stages of 12 partials (24.6 KB per block,
+// nine blocks per SM) measured best on the merge-stress shape (64 requests x
+// 24 heads x 256, 1..64 partials; per launch, back to back on inputs larger
+// than L2): 8 x 2 13.4 us, 10 x 2 12.4, 12 x 2 12.0, 14 x 2 13.2, 16 x 2 12.8,
+// 20 x 2 12.6, 8 x 3 12.7, 12 x 3 13.5.  Every column sums its partials in
+// increasing order with the same expressions as the decode kernel's fused
+// merge (mergerow::merge_cols), so the bits are the same.
 constexpr int kCols = 64;
-constexpr int kStageParts = 8;   // 16 KB of stages per block: every row of a
-constexpr int kStages = 2;       // 1,536-row launch is resident at once
+constexpr int kStageParts = 12;
+constexpr int kStages = 2;
 static_assert(kStages >= 1 && kStages <= 4, "the stage waits below cover up to four stages");
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {

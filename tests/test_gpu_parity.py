@@ -257,12 +257,13 @@ def test_lse_merge_stress_matches_unsplit_softmax(B):
 @pytest.mark.parametrize("D", [4, 12, 128, 132, 256, 260, 520])
 def test_lse_merge_head_dims_and_partial_counts(B, D):
     """Rows of any width (one or several 64-column passes, a ragged last one)
-    and partial counts on both sides of the kernel's eight-partial stages,
-    against the oracle's fp64 merge of the same fp32 partials."""
+    and partial counts on both sides of the kernel's twelve-partial stages and
+    of the eight-partial stages it had, against the oracle's fp64 merge of the
+    same fp32 partials."""
     dev = "cuda"
     g = torch.Generator(device=dev).manual_seed(D)
     H = 3
-    counts = [1, 2, 7, 8, 9, 15, 16, 17, 33, 64]
+    counts = [1, 2, 7, 8, 9, 11, 12, 13, 15, 16, 17, 23, 24, 25, 33, 64]
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
     P = int(offsets[-1])
     parts = torch.randn((P, H, D), generator=g, device=dev)
