@@ -404,12 +404,11 @@ __device__ __forceinline__ void merge_split_slice(const Params<kMaxUnits>& p, in
 }
 
 // Thread 0 of a CTA that has arrived at split unit `arrival` in generation
-// `gen`, with this unit's segment as its last: waits until the unit's last CTA
-// opens the next generation (every partial is then stored and visible).  If
-// no other CTA of the unit arrives for kSliceWaitNs while some have not, it
-// records itself as a leaver (the last CTA then merges every slice) and
-// returns false.  A CTA that finds every CTA arrived keeps waiting (the
-// opening follows the last arrival directly), up to wait_limit_ns.
+// `gen`, with this unit's segment as its last: waits until every CTA of the
+// unit has arrived (the count reaches n, or the last CTA has already opened
+// the next generation), so every partial is stored and visible.  If no other
+// CTA of the unit arrives for slice_wait_ns while some have not, it records
+// itself as a leaver (the last CTA then merges every slice) and returns false.
 __device__ __forceinline__ bool wait_unit_complete(unsigned long long* arrival, unsigned gen,
                                                    int n, uint64_t slice_wait_ns,
                                                    uint64_t wait_limit_ns, int32_t* status) {
@@ -417,18 +416,23 @@ __device__ __forceinline__ bool wait_unit_complete(unsigned long long* arrival, 
   uint64_t t_seen = t0;
   int seen = -1;
   while (true) {
-    const unsigned long long v = ptx::load_acquire_gpu(arrival);
-    if ((unsigned)(v >> 32) != gen) return true;
-    const uint64_t now = ptx::globaltimer_ns();
+    // Relaxed polls; the fence after the one that sees every arrival makes
+    // it an acquire of all of them (the last arrival is an acquire-release
+    // add, the opening add is in the release sequence of each).
+    const unsigned long long v = ptx::load_relaxed_gpu(arrival);
     const int count = (int)(v & 0xffffu);
+    if ((unsigned)(v >> 32) != gen || count == n) {
+      ptx::fence_acq_rel_gpu();
+      return true;
+    }
+    const uint64_t now = ptx::globaltimer_ns();
     if (count != seen) {
       seen = count;
       t_seen = now;
     }
-    if (count < n) {
-      if (now - t_seen > slice_wait_ns && ptx::atomic_cas_gpu(arrival, v, v + (1ull << 16)) == v)
-        return false;
-    } else if (now - t0 > wait_limit_ns) {
+    if (now - t_seen > slice_wait_ns && ptx::atomic_cas_gpu(arrival, v, v + (1ull << 16)) == v)
+      return false;
+    if (now - t0 > wait_limit_ns) {
       atomicOr(status, PA_STATUS_TIMEOUT);
       return false;
     }
@@ -1031,8 +1035,9 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         int leavers = 0;
         if (arrived == n) {
           leavers = (int)((prev >> 16) & 0xffffu);
-          // Count and leavers back to zero, generation + 1.
-          ptx::red_add_release_gpu(arrival, (1ull << 32) -
+          // Count and leavers back to zero, generation + 1 (a plain add: the
+          // waiting CTAs acquire the arrivals through it, see above).
+          ptx::red_add_relaxed_gpu(arrival, (1ull << 32) -
                                                 ((unsigned long long)leavers << 16) -
                                                 (unsigned long long)n);
           mode = leavers ? 2 : (participant ? 1 : 0);
