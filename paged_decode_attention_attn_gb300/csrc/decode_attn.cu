@@ -1014,14 +1014,15 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
     if (!single) {
       // Split unit: CTAs k0 .. k1 each stored a partial.  The barrier orders
       // every thread's partial before thread 0's acquire-release arrival,
-      // which publishes it at device scope.  The last CTA to arrive opens the
-      // arrival word's next generation; CTAs k0 .. k0 + S - 1 (S <= n - 1:
+      // which publishes it at device scope.  CTAs k0 .. k0 + S - 1 (S <= n - 1:
       // their page ranges end inside this unit, so it is their last segment)
-      // wait for that and each merges one of S slices of the unit's outputs,
-      // so the merge is spread over S SMs instead of loading every partial
-      // into one.  A CTA that gave up waiting leaves its slice to the last
-      // CTA, which then merges every slice (a slice merged twice gets the
-      // same bits).  The other CTAs leave at once.
+      // wait until all n have arrived and each merges one of S slices of the
+      // unit's outputs, so the merge is spread over S SMs instead of loading
+      // every partial into one; the last CTA to arrive resets the count and
+      // opens the word's next generation for the next call.  A CTA that gave
+      // up waiting leaves its slice to the last CTA, which then merges every
+      // slice (a slice merged twice gets the same bits).  The other CTAs
+      // leave at once.
       const int n = U.n_parts;
       const int S = split_slices(n);
       const int rank = (int)blockIdx.x - cta_of(pf, p.total_pages, p.grid);
@@ -1035,8 +1036,9 @@ __global__ void __launch_bounds__(Shape<kTensorCores>::kThreads, 1)
         int leavers = 0;
         if (arrived == n) {
           leavers = (int)((prev >> 16) & 0xffffu);
-          // Count and leavers back to zero, generation + 1 (a plain add: the
-          // waiting CTAs acquire the arrivals through it, see above).
+          // Count and leavers back to zero, generation + 1 (a plain add: a
+          // waiting CTA that reads it still acquires every arrival, which
+          // it follows in the word's order of modifications).
           ptx::red_add_relaxed_gpu(arrival, (1ull << 32) -
                                                 ((unsigned long long)leavers << 16) -
                                                 (unsigned long long)n);
