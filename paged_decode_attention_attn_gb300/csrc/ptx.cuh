@@ -110,10 +110,7 @@ __device__ __forceinline__ unsigned long long atomic_add_acq_rel_gpu(unsigned lo
                : "memory");
   return old;
 }
-// Device-scope add whose result is not needed, with release semantics.
-__device__ __forceinline__ void red_add_release_gpu(unsigned long long* p, unsigned long long v) {
-  asm volatile("red.release.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
-}
+// Device-scope add whose result is not needed, no ordering of its own.
 __device__ __forceinline__ void red_add_relaxed_gpu(unsigned long long* p, unsigned long long v) {
   asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
@@ -124,11 +121,6 @@ __device__ __forceinline__ unsigned long long load_relaxed_gpu(const unsigned lo
 }
 __device__ __forceinline__ void fence_acq_rel_gpu() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-__device__ __forceinline__ unsigned long long load_acquire_gpu(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
 }
 __device__ __forceinline__ unsigned long long atomic_cas_gpu(unsigned long long* p,
                                                              unsigned long long expected,
