@@ -890,6 +890,17 @@ def timeline_reading(tl):
             f"{what} {100 * split.get(worst, 0):.1f}%")
 
 
+def free_link_rate(staged_bytes, pairs, tl):
+    """Staged GB/s of the median single step among those whose every stage
+    copied at >= 90% of the leg's fastest stage (the link was not slowed by
+    other work during them); None if there is none."""
+    best = max([p[2] for p in pairs] + [((tl or {}).get("copy_GBps") or {}).get("max", 0.0)])
+    keep = [p[0] for p in pairs if p[2] >= CLEAN * best]
+    if not keep:
+        return None
+    return round(staged_bytes / statistics.median(keep) / 1e9, 2)
+
+
 def run_e2e(args, w, t, dev, D, B, host, compact=False, exact=None, tiled=False):
     """Staged route: host-owned history, host Q / new rows in, outputs out.
 
@@ -1025,6 +1036,7 @@ def run_e2e(args, w, t, dev, D, B, host, compact=False, exact=None, tiled=False)
             "step_ms_median": round(1e3 * statistics.median(step_s), 3),
             "step_ms": [round(1e3 * x, 3) for x in step_s],
             "route_h2d_GBps_median": round(staged_per_step / statistics.median(step_s) / 1e9, 2),
+            "route_h2d_GBps_median_free_link": free_link_rate(staged_per_step, pairs, tl),
             "probe_all_layers_GBps": [round(p[1], 2) for p in pairs],
             "stage_min_GBps": [round(p[2], 2) for p in pairs],
             "route_over_probe_median": round(statistics.median(ratios), 4),
@@ -1032,7 +1044,8 @@ def run_e2e(args, w, t, dev, D, B, host, compact=False, exact=None, tiled=False)
             "what": "a single step (drained) then one copy of every layer's history on one "
                     "stream, alternated; the ratio is the step's staged bytes over its time "
                     "against the probe right after it; stage_min_GBps is the slowest stage "
-                    "copy inside each single step",
+                    "copy inside each single step; the free-link rate takes the median of the "
+                    "single steps whose every stage copied at >= 90% of the leg's fastest",
         }
     if compact:
         exact_bytes = sum(run.get("n_rows", 0) * geo.row_bytes

@@ -89,3 +89,11 @@ def test_timeline_accounts_for_stages_that_copied_slowly():
     r["h2d_time_split"] = {"copying": 0.99, "slot_wait": 0.0, "host_gap": 0.01}
     text = bench.timeline_reading(r)
     assert "1 of 4 stages" in text and "1.5 ms" in text
+
+
+def test_free_link_rate_uses_single_steps_whose_stages_all_ran_at_link_rate():
+    # (step seconds, probe GB/s, slowest stage GB/s); the leg's fastest stage 210
+    pairs = [(0.040, 211.0, 205.0), (0.080, 211.0, 40.0), (0.042, 211.0, 200.0)]
+    tl = {"copy_GBps": {"max": 210.0}}
+    assert bench.free_link_rate(8.4e9, pairs, tl) == round(8.4e9 / 0.041 / 1e9, 2)
+    assert bench.free_link_rate(8.4e9, [(0.08, 211.0, 40.0)], tl) is None
