@@ -446,7 +446,9 @@ typedef struct {
  * compute stream's wait on it (attention enqueued after this call sees the
  * pages; a later stage's copies follow them on the H2D stream).  The caller
  * marks attention done (kv_mark_attention_done / kv_lease_attention_done)
- * after every kernel that reads resident pages, as for staged ones.  Refused
+ * after every kernel that reads resident pages, as for staged ones: a load
+ * waits only on attention already marked done, so every kernel that read the
+ * pages being replaced must be marked before the load is made.  Refused
  * before anything is enqueued (PA_ERR_INVALID): a page inside the staging
  * slots or outside the arena, n_rows outside 1..page_tokens, host rows not in
  * pinned host memory.  A failed submission quarantines the arena.  Works with
