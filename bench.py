@@ -561,7 +561,7 @@ def run_ours(args):
     torch.cuda.empty_cache()
 
     # ---- staged route, end to end through host buffers, every workload ----
-    e2e = e2e_compact = e2e_tiled = None
+    e2e = e2e_compact = e2e_tiled = e2e_planned = None
     bus = None
     staged = {}
     if not args.no_e2e:
@@ -578,6 +578,9 @@ def run_ours(args):
                     e2e_compact = finish_e2e(
                         run_e2e(args, wn, tn, dev, D, B, host, compact=True,
                                 exact=(summaries_exact(D, wn, tn, dev))), kvb, world)
+                if not wn.window and wn.n_tiles == 1:
+                    e2e_planned = finish_e2e(run_e2e_planned(args, wn, tn, dev, D, B, host),
+                                             kvb, world)
             if (name == "1x262144" and not args.no_bus_model_leg and rank == 0
                     and world == 1):
                 bus = bus_model_from_prefixes(args, wn, tn, host, dev, D)
@@ -635,6 +638,8 @@ def run_ours(args):
             line["e2e_compact"] = e2e_compact
         if e2e_tiled is not None:
             line["e2e_tiled"] = e2e_tiled
+        if e2e_planned is not None:
+            line["e2e_planned"] = e2e_planned
         if bus is not None:
             line["bus_model"] = bus
         if cpu is not None:
@@ -1072,6 +1077,74 @@ def run_e2e(args, w, t, dev, D, B, host, compact=False, exact=None, tiled=False)
     st.close()
     if store is not None:
         store.close()
+    return res
+
+
+def run_e2e_planned(args, w, t, dev, D, B, host, pool_gib=None):
+    """Planner-driven route, end to end through host buffers: the admission
+    planner keeps each context's hot pages in a device pool of ``pool_gib``
+    GiB (by default about half the history, rounded to whole GiB, at least 1;
+    a pool page holds a 64-token page of every layer), copied in once by
+    the arena, and every other page is staged per layer ("Staging without a
+    stall", section "Admission that does arithmetic").  Each context gets an
+    equal target of the pool's pages.  The same step as the staged legs (host
+    queries and new rows in, merged outputs out); the warm-up steps copy the
+    hot pages in, the timed steps stage only the cold ones."""
+    import numpy as np
+    import torch
+    geo = w.geometry
+    if pool_gib is None:
+        history = sum(w.pages_of(r) for r in range(w.batch)) * geo.page_tokens * geo.row_bytes
+        pool_gib = max(1, round(history * w.n_layers / 2 / (1 << 30)))
+    planner = B.Planner(pool_gib, n_layers=w.n_layers, max_contexts=w.batch,
+                        max_context_tokens=int(max(w.lengths)))
+    pool_pages, _ = planner.info()
+    target = pool_pages // w.batch
+    pd = D.PlannedDecode(w, t, host, planner, targets=[target] * w.batch,
+                         bursts=[0] * w.batch)
+    lengths = np.asarray(w.lengths, dtype=np.int64)
+    q_host = t["q"].cpu().pin_memory()
+    rows_host = t["new_rows"].cpu().pin_memory()
+    out_host = torch.empty(pd.out.shape, dtype=torch.float32).pin_memory()
+    lse_host = torch.empty(pd.lse.shape, dtype=torch.float32).pin_memory()
+
+    def step():
+        t["q"].copy_(q_host, non_blocking=True)
+        t["new_rows"].copy_(rows_host, non_blocking=True)
+        pd.step(lengths)
+        out_host.copy_(pd.out, non_blocking=True)
+        lse_host.copy_(pd.lse, non_blocking=True)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    pd.handle.drain()
+    torch.cuda.synchronize(dev)
+    s0 = pd.handle.stats()
+    steps = max(3, min(args.steps, 10))
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    pd.handle.drain()
+    torch.cuda.synchronize(dev)
+    secs = time.perf_counter() - t0
+    s1 = pd.handle.stats()
+    if pd.kernel_status() != 0:
+        raise RuntimeError("planned route kernel status non-zero")
+    staged = (s1.staged_bytes - s0.staged_bytes) // steps
+    loaded = (s1.loaded_bytes - s0.loaded_bytes) // steps
+    hot = sum(len(planner.resident(r)) for r in range(w.batch))
+    total = sum(w.pages_of(r) for r in range(w.batch))
+    h2d = q_host.numel() * 2 + rows_host.numel() * 2 + staged + loaded
+    d2h = out_host.numel() * 4 + lse_host.numel() * 4 + w.n_layers * w.batch * geo.row_bytes
+    res = {"unit": UNIT, "_secs": secs, "steps": steps,
+           "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+           "route": f"admission planner: {pool_gib} GiB device pool of hot pages copied in "
+                    "once, the rest staged per layer (2 arena slots), tail write-back",
+           "arena_bytes": int(pd.arena_buf.numel()),
+           "hot_pages": int(hot), "pages": int(total),
+           "staged_bytes_per_step": int(staged), "copied_in_bytes_per_step": int(loaded),
+           "h2d_GBps": round((staged + loaded) * steps / secs / 1e9, 2)}
+    pd.close()
     return res
 
 

@@ -44,6 +44,8 @@ def test_bench_line_has_the_contract_keys():
     for name, entry in wk.items():
         assert entry["value"] > 0 and 0 < entry["roofline"]["frac"] < 2, name
         assert entry["e2e"]["value"] > 0 and entry["e2e"]["timeline"]["stages"] > 0, name
+    pl = d["e2e_planned"]        # admission-planner window: hot pages resident, the rest staged
+    assert pl["value"] > 0 and pl["hot_pages"] > 0 and pl["copied_in_bytes_per_step"] == 0
     bm = d["bus_model"]
     assert len(bm["points"]) == 4 and bm["fit"]["link_GBps"] > 0
     assert "worst_error_pct" in bm and bm["legs"]["per_leg"]
