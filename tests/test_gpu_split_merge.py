@@ -86,3 +86,25 @@ def test_split_units_match_the_oracle_when_merged_by_the_last_cta(mods):
     ref = oracle_request(w, t, 0, 0, gather_on_device=True)
     assert_close_to_oracle(dec.o.tile_out[0, 0], dec.o.tile_lse[0, 0], dec.o.out[0, 0],
                            dec.o.lse[0, 0], ref, w.tiles[0], "1x32768 leavers")
+
+
+@pytest.mark.parametrize("leave", [False, True], ids=["merged-by-slices", "left-to-last-cta"])
+def test_one_unit_split_over_every_cta(mods, leave):
+    """One kv head, eight query heads, one 131,072-token tile: the single unit
+    spans every CTA of the grid (as many partials as a split unit can have),
+    merged in slices or by the last CTA alone, against the fp64 oracle."""
+    from parity_utils import assert_close_to_oracle, oracle_request
+    B, D = mods
+    geo = wl.Geometry(n_q_heads=8, n_kv_heads=1)
+    w = wl.custom([131072], [[(0, 131072)]], seed=29, n_layers=1, geometry=geo)
+    t = wl.materialize(w, "cuda")
+    dec = D.ResidentDecode(w, t)
+    if leave:
+        B.test_slice_wait(0)
+    dec.layer(0)
+    torch.cuda.synchronize()
+    assert dec.kernel_status() == 0
+    assert (leavers(dec) > 0) == leave
+    ref = oracle_request(w, t, 0, 0, gather_on_device=True)
+    assert_close_to_oracle(dec.o.tile_out[0, 0], dec.o.tile_lse[0, 0], dec.o.out[0, 0],
+                           dec.o.lse[0, 0], ref, w.tiles[0], "1 kv head x 131072")
