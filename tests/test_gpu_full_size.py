@@ -21,8 +21,10 @@ pytestmark = pytest.mark.gpu
 
 FULL = {
     "4x31744": (wl.four_requests_31744, [(0, 1), (15, 3)]),
-    "1x262144": (wl.one_request_262144, [(7, 0)]),
+    "1x262144": (wl.one_request_262144, [(7, 0), (15, 0)]),
     "ragged-window": (wl.ragged_window, [(3, "longest"), (12, "shortest")]),
+    "1x32768": (lambda n_layers=16: wl.uniform(1, 32768, 32768, n_layers=n_layers),
+                [(0, 0), (9, 0)]),
 }
 
 
