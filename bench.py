@@ -753,6 +753,18 @@ def merge_arm(dev, B, rounds=7, per_round=48, copies=4):
         torch.cuda.synchronize(dev)
         per_launch.append(e0.elapsed_time(e1) / per_round)
     ms = statistics.median(per_launch)
+    # the same launches one at a time, each between its own events (adds the
+    # launch latency, which back-to-back launches hide; the event clock ticks
+    # in ~2 us steps)
+    alone = []
+    for k in range(2 * per_round // 3):
+        op, lp = parts[k % copies]
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        B.lse_merge(op, lp, off_d, out, lse, stream=stream)
+        e1.record(stream)
+        e1.synchronize()
+        alone.append(e0.elapsed_time(e1))
     n_parts = int(offsets[-1])
     # partials read once (outputs and LSEs), offsets read, merged rows written
     nbytes = (n_parts * H * (Dh + 1) + n_req * H * (Dh + 1)) * 4 + (n_req + 1) * 4
@@ -760,6 +772,7 @@ def merge_arm(dev, B, rounds=7, per_round=48, copies=4):
     peak, peak_kind = hbm_peak()
     return {"value": round(gbs, 1), "unit": "GB/s", "kernel": "lse_merge_kernel",
             "mean_launch_us": round(ms * 1e3, 2), "launches": rounds * per_round,
+            "alone_launch_us_median": round(statistics.median(alone) * 1e3, 2),
             "bytes_per_launch": nbytes, "partials": n_parts, "requests": n_req,
             "frac_of_hbm_peak": round(gbs / peak, 4), "peak_kind": peak_kind,
             "timing": f"events around {per_round} back-to-back launches, median of {rounds}",
