@@ -73,6 +73,8 @@ constexpr int kSmemUsed = kSmemMisc + 64;
 constexpr int kSmemAlloc = kSmemUsed + 1024;             // slack to align to 1 KiB
 constexpr int kMaxUnitsLarge = 1024;
 constexpr int kMaxUnitsSmall = 64;
+constexpr int kWidePages = 32;     // pages per SM from which a launch leaves SMs idle
+constexpr int kWideGridPct = 90;   // share of the SMs such a launch runs on
 constexpr int kSegmentCharge = 6;  // pages charged per segment when CTAs' shares are cut (measured: 3-8 best)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;         // 2 s per wait
 // A split unit's merge reads up to kMaxPartsPerLane partials per lane of a
@@ -175,6 +177,20 @@ __host__ __device__ __forceinline__ int split_slices(int n) {
 
 __host__ __device__ __forceinline__ int unit_pages(int tok_start, int tok_end) {
   return tok_end > tok_start ? (tok_end + kPage - 1) / kPage - tok_start / kPage : 0;
+}
+
+// CTAs of a launch of `total` flattened pages on a device of `sms` SMs.  A
+// launch of at least kWidePages pages per SM runs on kWideGridPct percent of
+// the SMs: with HBM saturated, fewer, longer streams finish sooner.  Measured
+// per launch on one box (grids 152 / 144 / 136 / 128): 4 x 31,744 tokens 78.6
+// / 77.9 / 78.1 / 78.1 us, 1 x 262,144 in 8 tiles 157.5 / 155.7 / 154.8 /
+// 155.6 us, the ragged window workload 462.4 / 459.8 / 459.2 / 460.3 us;
+// smaller launches keep every SM (1 x 32,768: 25.4 us on 152, 25.7 on 136;
+// 2 x 32,768 within 0.1% from 120 to 152).
+__host__ __forceinline__ int launch_grid(long long total, int sms) {
+  if (total <= 0) return 1;
+  if (total >= (long long)kWidePages * sms) return std::max(1, sms * kWideGridPct / 100);
+  return (int)std::min<long long>(sms, total);
 }
 
 // CTA whose page range [k P / grid, (k+1) P / grid) holds flattened page p.
@@ -1316,7 +1332,7 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
       total += np;
       PA_REQUIRE(total < (1ll << 31), "too many pages in one launch");
     }
-    const int grid = total > 0 ? (int)std::min<long long>(sms, total) : 1;
+    const int grid = launch_grid(total, sms);
     int part_cursor = 0;
     for (size_t i = u0; i < u0 + n; ++i) {
       const int np = unit_pages(units[i].tok_start, units[i].tok_end);

@@ -337,7 +337,8 @@ def test_other_head_geometries_match_oracle(B, D, hq, hkv):
 def split_counts(lengths, tiles, n_kv_heads, sms, charge=6, page=64):
     """CTAs covering each (request, tile, kv head) unit when a launch's pages,
     each non-empty unit preceded by `charge` pages of bookkeeping, are cut
-    into `sms` equal shares (the decode launch's work split)."""
+    into equal shares, one per CTA (the decode launch's work split; a launch
+    of at least 32 pages per SM runs on 90% of the SMs)."""
     units = [(s, e) for _ in range(n_kv_heads) for tl in tiles for (s, e) in tl]
     spans, total = [], 0
     for s, e in units:
@@ -346,7 +347,7 @@ def split_counts(lengths, tiles, n_kv_heads, sms, charge=6, page=64):
             total += charge
             spans.append((total, n))
         total += n
-    grid = min(sms, total)
+    grid = sms * 90 // 100 if total >= 32 * sms else min(sms, total)
     cta = lambda p: ((p + 1) * grid - 1) // total
     return [cta(f + n - 1) - cta(f) + 1 for f, n in spans]
 
