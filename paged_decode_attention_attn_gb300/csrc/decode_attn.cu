@@ -10,13 +10,13 @@
 //
 //  * Work = (tile, kv head) units, each a run of 64-token pages.  All units'
 //    pages are laid end to end and cut into one contiguous page range per CTA
-//    (persistent grid, one CTA per SM), so every SM streams the same number of
-//    pages whatever the mix of lengths.  A unit that spans several CTAs leaves
-//    one partial (max, sum, unnormalised output) per CTA; once the last of
-//    them has arrived, the unit's CTAs merge the partials in slices of the
-//    output, each slice with a fixed summation order, so the result does not
-//    depend on timing, on which CTA merges which slice, or on where pages sit
-//    physically.
+//    (persistent grid, one CTA per SM; 90% of the SMs for launches of many
+//    pages per SM), so every CTA streams the same number of pages whatever the
+//    mix of lengths.  A unit that spans several CTAs leaves one partial (max,
+//    sum, unnormalised output) per CTA; once the last of them has arrived, the
+//    unit's CTAs merge the partials in slices of the output, each slice with a
+//    fixed summation order, so the result does not depend on timing, on which
+//    CTA merges which slice, or on where pages sit physically.
 //  * One producer warp streams pages with TMA: per page the K slice and the V
 //    slice of one kv head (64 rows x 512 B each, row stride 4 KiB) as eight
 //    64x64 boxes with the 128-byte swizzle, into a 3-stage mbarrier ring
