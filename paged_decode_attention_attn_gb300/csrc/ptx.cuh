@@ -114,13 +114,11 @@ __device__ __forceinline__ unsigned long long atomic_add_acq_rel_gpu(unsigned lo
 __device__ __forceinline__ void red_add_relaxed_gpu(unsigned long long* p, unsigned long long v) {
   asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
-__device__ __forceinline__ unsigned long long load_relaxed_gpu(const unsigned long long* p) {
+// Device-scope load with acquire semantics.
+__device__ __forceinline__ unsigned long long load_acquire_gpu(const unsigned long long* p) {
   unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 __device__ __forceinline__ unsigned long long atomic_cas_gpu(unsigned long long* p,
                                                              unsigned long long expected,
