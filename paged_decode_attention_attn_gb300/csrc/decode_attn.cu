@@ -1130,20 +1130,12 @@ size_t workspace_bytes(int B, int T, int Hkv) {
 
 template <int N, bool TC>
 cudaError_t launch(const CUtensorMap& tmap, const Params<N>& prm, int grid, cudaStream_t stream) {
-  static std::mutex mu;
-  static bool configured[64] = {false};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static PerContext smem_limit;   // the attribute lives in the context
+  cudaError_t e = smem_limit.apply([] {
+    return cudaFuncSetAttribute(paged_decode_kernel<N, TC>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  });
   if (e != cudaSuccess) return e;
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && !configured[dev]) {
-      e = cudaFuncSetAttribute(paged_decode_kernel<N, TC>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-      if (e != cudaSuccess) return e;
-      configured[dev] = true;
-    }
-  }
   e = launch_dependent(paged_decode_kernel<N, TC>, dim3(grid), dim3(Shape<TC>::kThreads),
                        kSmemAlloc, stream, tmap, prm);
   if (e != cudaSuccess) return e;
@@ -1455,35 +1447,6 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB per device
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-using CtxGetCurrentFn = CUresult (*)(CUcontext*);
-using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
-
-// Id of the CUDA context current on this thread (unique for the process's
-// lifetime, so a context destroyed and made again gets a new one); false if
-// no context is current or the driver cannot say.
-bool current_context_id(unsigned long long* id) {
-  static CtxGetCurrentFn get_current = nullptr;
-  static CtxGetIdFn get_id = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      get_current = reinterpret_cast<CtxGetCurrentFn>(ptr);
-    ptr = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      get_id = reinterpret_cast<CtxGetIdFn>(ptr);
-  });
-  if (!get_current || !get_id) return false;
-  CUcontext ctx = nullptr;
-  if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
-  return get_id(ctx, id) == CUDA_SUCCESS;
-}
-
 struct ScratchAddress {
   unsigned long long ctx_id = 0;
   void* ptr = nullptr;
@@ -1506,7 +1469,7 @@ int noalloc_scratch(void** out) {
   if (e != cudaSuccess) return pa::fail(PA_ERR_CUDA, "cudaGetDevice failed: %s", cudaGetErrorString(e));
   if (dev < 0 || dev >= 64) return pa::fail(PA_ERR_INVALID, "device index %d out of range", dev);
   unsigned long long id = 0;
-  bool have_id = current_context_id(&id);
+  bool have_id = pa::current_context_id(&id);
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
   ScratchAddress& c = g_noalloc_addr[dev];
   if (!have_id || c.ptr == nullptr || c.ctx_id != id) {
@@ -1516,7 +1479,7 @@ int noalloc_scratch(void** out) {
       return pa::fail(PA_ERR_CUDA, "cudaGetSymbolAddress of the scratch array failed: %s",
                       cudaGetErrorString(r));
     // The lookup makes the device's primary context current if none was.
-    if (!have_id) have_id = current_context_id(&id);
+    if (!have_id) have_id = pa::current_context_id(&id);
     c.ptr = have_id ? ptr : nullptr;
     c.ctx_id = have_id ? id : 0;
     *out = ptr;

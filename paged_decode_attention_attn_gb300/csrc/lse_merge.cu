@@ -205,10 +205,14 @@ extern "C" int lse_merge(const float* out_parts, const float* lse_parts,
              "out and out_parts must be 16-byte aligned");
   const long long rows = (long long)B * H;
   PA_REQUIRE(rows < (1ll << 31), "too many (request, head) pairs");
-  // Many 16 KB blocks per SM: ask for the largest shared-memory carveout.
-  PA_CHECK_CUDA(cudaFuncSetAttribute(pa::merge::lse_merge_kernel,
-                                     cudaFuncAttributePreferredSharedMemoryCarveout,
-                                     cudaSharedmemCarveoutMaxShared));
+  // Many 24.7 KB blocks per SM: ask for the largest shared-memory carveout
+  // (once per context).
+  static pa::PerContext carveout;
+  PA_CHECK_CUDA(carveout.apply([] {
+    return cudaFuncSetAttribute(pa::merge::lse_merge_kernel,
+                                cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+  }));
   PA_CHECK_CUDA(pa::launch_dependent(pa::merge::lse_merge_kernel, dim3((unsigned)rows),
                                      dim3(pa::merge::kCols), 0, stream, out_parts, lse_parts,
                                      part_offsets, B, H, D, out, lse));
