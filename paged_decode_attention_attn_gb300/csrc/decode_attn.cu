@@ -186,8 +186,9 @@ __host__ __device__ __forceinline__ int unit_pages(int tok_start, int tok_end) {
 // / 77.9 / 78.1 / 78.1 us, 1 x 262,144 in 8 tiles 157.5 / 155.7 / 154.8 /
 // 155.6 us, the ragged window workload 462.4 / 459.8 / 459.2 / 460.3 us;
 // smaller launches keep every SM (1 x 32,768: 25.4 us on 152, 25.7 on 136;
-// 2 x 32,768 within 0.1% from 120 to 152).  Launches of many short units can
-// lose a little (16 x 8,192: 80.7 -> 81.2 us), 3 x 32,768 gains 0.35%.
+// 2 x 32,768 within 0.1% from 120 to 152).  Of the other launches above the
+// threshold measured, 3 x 32,768, 8 x 16,384 and 64 x 2,048 gain 0.2-1.6% and
+// 16 x 8,192 loses 0.6%.
 __host__ __forceinline__ int launch_grid(long long total, int sms) {
   if (total <= 0) return 1;
   if (total >= (long long)kWidePages * sms) return std::max(1, sms * kWideGridPct / 100);
