@@ -194,9 +194,17 @@ __host__ __device__ __forceinline__ int unit_pages(int tok_start, int tok_end) {
 // 2 x 32,768 within 0.1% from 120 to 152).  Of the other launches above the
 // threshold measured, 3 x 32,768, 8 x 16,384 and 64 x 2,048 gain 0.2-1.6% and
 // 16 x 8,192 loses 0.6%.
-__host__ __forceinline__ int launch_grid(long long total, int sms) {
+// The narrowed grid is a multiple of the kv-head count, so the CTAs at the
+// same offset of each kv head's block of units still stream the same pages
+// at the same time (with 4 kv heads, 129 CTAs took the bench workload to
+// 80.6 us against 77.1 on 136 and 77.1 on 144).
+__host__ __forceinline__ int launch_grid(long long total, int sms, int n_kv_heads) {
   if (total <= 0) return 1;
-  if (total >= (long long)kWidePages * sms) return std::max(1, sms * kWideGridPct / 100);
+  if (total >= (long long)kWidePages * sms) {
+    int grid = std::max(1, sms * kWideGridPct / 100);
+    if (grid >= n_kv_heads) grid -= grid % n_kv_heads;
+    return grid;
+  }
   return (int)std::min<long long>(sms, total);
 }
 
@@ -1330,7 +1338,7 @@ int run(bool tensor_cores, const void* q, const void* pool, int64_t pool_pages,
       total += np;
       PA_REQUIRE(total < (1ll << 31), "too many pages in one launch");
     }
-    const int grid = launch_grid(total, sms);
+    const int grid = launch_grid(total, sms, n_kv_heads);
     int part_cursor = 0;
     for (size_t i = u0; i < u0 + n; ++i) {
       const int np = unit_pages(units[i].tok_start, units[i].tok_end);
