@@ -194,18 +194,18 @@ __host__ __device__ __forceinline__ int unit_pages(int tok_start, int tok_end) {
 // 2 x 32,768 within 0.1% from 120 to 152).  Of the other launches above the
 // threshold measured, 3 x 32,768, 8 x 16,384 and 64 x 2,048 gain 0.2-1.6% and
 // 16 x 8,192 loses 0.6%.
-// The narrowed grid is a multiple of the kv-head count, so the CTAs at the
-// same offset of each kv head's block of units still stream the same pages
-// at the same time (with 4 kv heads, 129 CTAs took the bench workload to
-// 80.6 us against 77.1 on 136 and 77.1 on 144).
+// The grid is rounded down to a multiple of the kv-head count (when it holds
+// at least one CTA per kv head), so the CTAs at the same offset of each kv
+// head's block of units stream the same pages at the same time: with 4 kv
+// heads, 129 CTAs took the bench workload to 80.6 us against 77.1 on 136 and
+// 77.1 on 144; with 6 kv heads, 150 CTAs instead of 152 took 1 x 32,768
+// tokens from 34.95 to 34.05 us and 2 x 16,384 from 34.64 to 33.94 us.
 __host__ __forceinline__ int launch_grid(long long total, int sms, int n_kv_heads) {
   if (total <= 0) return 1;
-  if (total >= (long long)kWidePages * sms) {
-    int grid = std::max(1, sms * kWideGridPct / 100);
-    if (grid >= n_kv_heads) grid -= grid % n_kv_heads;
-    return grid;
-  }
-  return (int)std::min<long long>(sms, total);
+  int grid = total >= (long long)kWidePages * sms ? std::max(1, sms * kWideGridPct / 100)
+                                                  : (int)std::min<long long>(sms, total);
+  if (grid >= n_kv_heads) grid -= grid % n_kv_heads;
+  return grid;
 }
 
 // CTA whose page range [k P / grid, (k+1) P / grid) holds flattened page p.

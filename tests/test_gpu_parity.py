@@ -338,8 +338,8 @@ def split_counts(lengths, tiles, n_kv_heads, sms, charge=6, page=64):
     """CTAs covering each (request, tile, kv head) unit when a launch's pages,
     each non-empty unit preceded by `charge` pages of bookkeeping, are cut
     into equal shares, one per CTA (the decode launch's work split; a launch
-    of at least 32 pages per SM runs on 90% of the SMs, rounded down to a
-    multiple of the kv-head count)."""
+    of at least 32 pages per SM runs on 90% of the SMs; the grid is rounded
+    down to a multiple of the kv-head count)."""
     units = [(s, e) for _ in range(n_kv_heads) for tl in tiles for (s, e) in tl]
     spans, total = [], 0
     for s, e in units:
@@ -348,11 +348,9 @@ def split_counts(lengths, tiles, n_kv_heads, sms, charge=6, page=64):
             total += charge
             spans.append((total, n))
         total += n
-    if total >= 32 * sms:
-        grid = sms * 90 // 100
-        grid -= grid % n_kv_heads if grid >= n_kv_heads else 0
-    else:
-        grid = min(sms, total)
+    grid = sms * 90 // 100 if total >= 32 * sms else min(sms, total)
+    if grid >= n_kv_heads:
+        grid -= grid % n_kv_heads
     cta = lambda p: ((p + 1) * grid - 1) // total
     return [cta(f + n - 1) - cta(f) + 1 for f, n in spans]
 
